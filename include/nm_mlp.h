@@ -1,0 +1,164 @@
+/*
+ * nm_mlp.h -- C ABI of libnmmlp: batched inference of a small fused FP16 MLP
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * The problem statement these calls follow comes from the page "Profiling
+ * neural material inference":
+ *  - "Experiment setup": one dispatch evaluates a batch of inputs, each
+ *    through the complete eight-affine-layer network (E1/E2/E3/F/S/D/H/O);
+ *    the timing covers the whole inference pass.
+ *  - "Bad versus good activation": between layers the FP16 activation
+ *    value = max(value, value * half(0.01)) is applied to the whole vector.
+ *  - "Row-major versus InferencingOptimal weights": the network's canonical
+ *    weights are FP16 row-major matrices; before inference they are converted
+ *    once into an opaque, device-dependent layout whose size the application
+ *    queries; the conversion changes neither the network nor the activation
+ *    and is paid only when the weights change.
+ * and from "Working with Cooperative Matrices", "Hardware Constraints and
+ * Capabilities": FP16 operands with FP32 accumulation, and 16-byte aligned
+ * addresses for every load and store of matrix data.
+ *
+ * Arithmetic of one evaluation (layer l = 0..L-1, K = d_l, N = d_{l+1}):
+ *   acc[o] = sum_k x[k] * W_l[o][k]          FP16 x FP16 products, FP32 sum
+ *   v[o]   = acc[o] + b_l[o]                  FP32
+ *   h[o]   = fp16_rn(v[o])                    round to nearest even
+ *   h[o]   = max(h[o], h[o] * half(0.01))     FP16, for every layer but the last
+ * The tensor cores sum the K products in an order and with an internal
+ * precision of their own, so results match a k-ordered FP32 sum to within
+ * |gpu - cpu| <= 1e-2 + 1e-2 |cpu| per element, and bit for bit wherever
+ * every partial sum is exact in FP32.
+ *
+ * Conventions for every call:
+ *  - Device pointers are CUDA device addresses on the device that was current
+ *    when nm_mlp_create ran; that device must be current for every later call.
+ *  - Every matrix pointer must be 16-byte aligned; matrices are row-major and
+ *    tightly packed (row stride = width * 2 bytes).
+ *  - nm_mlp_pack_weights, nm_mlp_unpack_weights and nm_mlp_infer are
+ *    stream-ordered and asynchronous: they enqueue work on `stream` and return;
+ *    the caller keeps the buffers alive until the stream has passed the call.
+ *    A NULL stream is the legacy default stream.
+ *  - A handle is not thread-safe. Infers on different streams may overlap if
+ *    their outputs do not.
+ *  - Errors are returned, never printed or raised. Argument errors are found
+ *    on the host before anything is enqueued.
+ */
+#ifndef NM_MLP_H
+#define NM_MLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (the same object as cudaStream_t / CUstream). */
+typedef struct CUstream_st *nm_stream;
+
+/* Opaque network handle: layer dims, the packed weight blob in device memory
+ * and a device status word. */
+typedef struct nm_mlp nm_mlp;
+
+typedef enum nm_status {
+    NM_OK = 0,
+    NM_ERR_INVALID_ARG = 1,  /* NULL / misaligned pointer, negative n, bad dims array */
+    NM_ERR_UNSUPPORTED = 2,  /* dims outside the supported set, or not an sm_103 device */
+    NM_ERR_NOT_PACKED = 3,   /* infer or unpack before nm_mlp_pack_weights */
+    NM_ERR_OOM = 4,          /* device allocation failed */
+    NM_ERR_CUDA = 5,         /* a CUDA runtime/driver call or launch failed */
+    NM_ERR_TIMEOUT = 6       /* a bounded wait inside a kernel gave up (see nm_mlp_device_status) */
+} nm_status;
+
+/* Kernel variants. NM_VARIANT_FUSED is the product path; the other two are
+ * the page's two performance cliffs, kept as measured ablations. All three
+ * produce bit-identical outputs. */
+typedef enum nm_variant {
+    /* Packed weights staged once per CTA into shared memory; packed half2
+     * activation ("Row-major versus InferencingOptimal weights", optimal
+     * layout; "Bad versus good activation", good form). */
+    NM_VARIANT_FUSED = 0,
+    /* Ablation of the weight layout: for every 128-sample tile and every
+     * layer the B operand is rebuilt in shared memory from the row-major
+     * weights in global memory instead of being staged once packed
+     * ("Row-major versus InferencingOptimal weights", row-major side). */
+    NM_VARIANT_ROWMAJOR_WEIGHTS = 1,
+    /* Ablation of the activation: the epilogue walks the FP16 values one by
+     * one with a dynamic index and a branch, if (h < 0) h *= half(0.01)
+     * ("Bad versus good activation", bad form). */
+    NM_VARIANT_SCALAR_ACTIVATION = 2
+} nm_variant;
+
+/* Version of this ABI (bumped on any incompatible change). */
+int32_t nm_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *nm_status_str(nm_status s);
+
+/* Create a network of L = n_dims - 1 affine layers with widths
+ * dims[0] (inputs) .. dims[L] (outputs).
+ * Supported: 1 <= L <= 16 and every width a multiple of 16 in [16, 256].
+ * Allocates the packed blob and a status word on the current device (the
+ * handle owns them; nm_mlp_destroy frees them).
+ * Errors: NM_ERR_INVALID_ARG (dims or out NULL, n_dims < 2),
+ * NM_ERR_UNSUPPORTED (widths/depth outside the set above, or the current
+ * device is not compute capability 10.3), NM_ERR_OOM, NM_ERR_CUDA.
+ * On error *out is set to NULL. */
+nm_status nm_mlp_create(const int32_t *dims, int32_t n_dims, nm_mlp **out);
+
+/* Size in bytes of the packed (device-private) weight blob -- the analogue of
+ * the page's size query for the InferencingOptimal layout. */
+nm_status nm_mlp_packed_size(const nm_mlp *h, size_t *bytes);
+
+/* One-time conversion of the canonical weights into the packed layout
+ * ("Row-major versus InferencingOptimal weights").
+ * W: host array of L device pointers; W[l] is FP16 [dims[l+1]][dims[l]]
+ *    row-major (row o holds the weights of output o).
+ * b: host array of L device pointers; b[l] is FP16 [dims[l+1]].
+ * The packed bits are a permutation of the input bits (no arithmetic).
+ * Errors: NM_ERR_INVALID_ARG (NULL or misaligned pointer), NM_ERR_CUDA. */
+nm_status nm_mlp_pack_weights(nm_mlp *h, const void *const *W, const void *const *b,
+                              nm_stream stream);
+
+/* Inverse of nm_mlp_pack_weights, into caller buffers of the same shapes.
+ * Errors: NM_ERR_INVALID_ARG, NM_ERR_NOT_PACKED, NM_ERR_CUDA. */
+nm_status nm_mlp_unpack_weights(const nm_mlp *h, void *const *W, void *const *b,
+                                nm_stream stream);
+
+/* Device address of the packed blob (read-only; for byte-for-byte checks of
+ * the packer). Valid until nm_mlp_destroy. */
+nm_status nm_mlp_packed_blob(const nm_mlp *h, const void **blob);
+
+/* Evaluate the network on n inputs ("Experiment setup": one dispatch).
+ * in:  device FP16 [n][dims[0]] row-major.   out: device FP16 [n][dims[L]].
+ * n == 0 is a no-op. Rows of `out` beyond n are never written.
+ * Errors: NM_ERR_INVALID_ARG (NULL/misaligned pointers, n < 0 or n >= 2^38),
+ * NM_ERR_NOT_PACKED, NM_ERR_UNSUPPORTED (the network does not fit the
+ * selected variant's shared-memory budget), NM_ERR_CUDA (launch failure).
+ * A kernel-side wait that gives up is reported by nm_mlp_device_status. */
+nm_status nm_mlp_infer(nm_mlp *h, const void *in, int64_t n, void *out, nm_stream stream);
+
+/* Select the kernel variant used by later nm_mlp_infer calls.
+ * Errors: NM_ERR_INVALID_ARG for an unknown variant. */
+nm_status nm_mlp_set_variant(nm_mlp *h, nm_variant v);
+
+/* Synchronise `stream`, then read and clear the handle's device status word.
+ * Returns NM_ERR_TIMEOUT if any kernel of this handle gave up a bounded wait
+ * since the last call (its outputs are then undefined), NM_ERR_CUDA if the
+ * synchronisation reported an error, else NM_OK. */
+nm_status nm_mlp_device_status(nm_mlp *h, nm_stream stream);
+
+/* Limit, in nanoseconds, of every wait inside the inference kernels
+ * (default 2,000,000,000). A wait that exceeds it sets the status word and
+ * the kernel winds down (drains its copies in flight, frees its tensor
+ * memory) and returns. Tests set a tiny limit to exercise that path. */
+nm_status nm_mlp_set_wait_limit(nm_mlp *h, uint64_t nanoseconds);
+
+/* Free the handle and its device memory (synchronises the device first).
+ * NULL is a no-op. */
+void nm_mlp_destroy(nm_mlp *h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NM_MLP_H */

@@ -1,0 +1,385 @@
+// nm_api.cu -- the C ABI of libnmmlp (declared in include/nm_mlp.h) and the
+// weight pack/unpack kernels.
+//
+// Pack ("Profiling neural material inference", "Row-major versus
+// InferencingOptimal weights": a one-time conversion of the canonical FP16
+// row-major matrices into an opaque device layout) is a pure permutation:
+// each thread moves one 16-byte chunk (8 weights of one row) from the
+// row-major matrix to its swizzled place in the packed blob, and biases are
+// copied unchanged behind the weight images. Unpack is the same map run
+// backwards.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "nm_internal.h"
+#include "nm_mlp.h"
+
+namespace nm {
+
+__global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackParams p, int unpack) {
+  const uint32_t total_w = p.chunk_start[p.L];
+  const uint32_t total = total_w + p.bias_chunk_start[p.L];
+  for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < total; g += gridDim.x * blockDim.x) {
+    if (g < total_w) {
+      int l = 0;
+      while (g >= p.chunk_start[l + 1]) ++l;
+      const uint32_t idx = g - p.chunk_start[l];
+      const int K = p.dims[l], N = p.dims[l + 1], kc = K >> 3;
+      const int n = static_cast<int>(idx / static_cast<uint32_t>(kc));
+      const int col = static_cast<int>(idx - static_cast<uint32_t>(n * kc)) << 3;
+      uint32_t off;
+      int w, k0;
+      locate(static_cast<uint32_t>(N), K, col, off, w, k0);
+      const uint32_t dst =
+          p.w_off[l] + off + swz(static_cast<uint32_t>(n * 2 * w + (col - k0) * 2), w);
+      uint4* packed = reinterpret_cast<uint4*>(p.blob + dst);
+      uint4* rowmajor = reinterpret_cast<uint4*>(p.rm_w[l] + static_cast<size_t>(n) * K + col);
+      if (!unpack)
+        *packed = __ldg(rowmajor);
+      else
+        *rowmajor = *packed;
+    } else {
+      const uint32_t gb = g - total_w;
+      int l = 0;
+      while (gb >= p.bias_chunk_start[l + 1]) ++l;
+      uint4* packed = reinterpret_cast<uint4*>(p.blob + p.bias_off) + gb;
+      uint4* rowmajor = reinterpret_cast<uint4*>(p.rm_b[l]) + (gb - p.bias_chunk_start[l]);
+      if (!unpack)
+        *packed = __ldg(rowmajor);
+      else
+        *rowmajor = *packed;
+    }
+  }
+}
+
+cudaError_t launch_pack(const PackParams& p, bool unpack, int num_sms, cudaStream_t stream) {
+  const uint32_t total = p.chunk_start[p.L] + p.bias_chunk_start[p.L];
+  int grid = static_cast<int>((total + 255u) / 256u);
+  if (grid > 4 * num_sms) grid = 4 * num_sms;
+  if (grid < 1) grid = 1;
+  pack_kernel<<<grid, 256, 0, stream>>>(p, unpack ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace nm
+
+using nm::FusedParams;
+using nm::PackParams;
+
+struct nm_mlp {
+  FusedParams params;  // kernel parameter block (dims, offsets, tensor maps)
+  int L = 0;
+  int32_t dims[nm::kMaxLayers + 1] = {};
+  size_t blob_size = 0;
+  uint8_t* blob = nullptr;       // packed weight images + FP16 biases (device)
+  uint32_t* status = nullptr;    // device status word
+  uint16_t* mirror = nullptr;    // row-major weights + biases for the row-major ablation
+  uint32_t rm_b_off[nm::kMaxLayers] = {};
+  size_t mirror_elems = 0;
+  bool packed = false;
+  bool mirror_valid = false;
+  int variant = nm::kVarFused;
+  uint64_t wait_ns = 2000000000ull;
+  int device = 0;
+  int num_sms = 0;
+  uint32_t smem_optin = 0;
+  const void* map_in = nullptr;
+  const void* map_out = nullptr;
+  int64_t map_n = -1;
+};
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+nm_status get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? NM_OK : NM_ERR_CUDA;
+}
+
+// 2-D map over a row-major FP16 [rows][width] matrix; box = [box_rows][box_w]
+// with the swizzle that matches a box_w-wide segment.
+nm_status encode_map(CUtensorMap* m, const void* ptr, int width, int64_t rows, int box_w,
+                     int box_rows) {
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(width) * 2u};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_w), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estride[2] = {1, 1};
+  const CUtensorMapSwizzle sw = box_w == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : box_w == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_32B;
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), gdim,
+                              gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NM_OK : NM_ERR_CUDA;
+}
+
+nm_status encode_io_maps(nm_mlp* h, const void* in, void* out, int64_t n) {
+  if (h->map_in == in && h->map_out == out && h->map_n == n) return NM_OK;
+  nm_status st = get_encoder();
+  if (st != NM_OK) return st;
+  FusedParams& p = h->params;
+  std::memset(p.tm_in, 0, sizeof(p.tm_in));
+  std::memset(p.tm_out, 0, sizeof(p.tm_out));
+  int w[16], k0[16];
+  int ns = nm::segments(h->dims[0], w, k0);
+  for (int s = 0; s < ns; ++s) {
+    st = encode_map(&p.tm_in[nm::swizzle_kind(w[s])], in, h->dims[0], n, w[s], nm::kTileM);
+    if (st != NM_OK) return st;
+  }
+  ns = nm::segments(h->dims[h->L], w, k0);
+  for (int s = 0; s < ns; ++s) {
+    st = encode_map(&p.tm_out[nm::swizzle_kind(w[s])], out, h->dims[h->L], n, w[s], 32);
+    if (st != NM_OK) return st;
+  }
+  h->map_in = in;
+  h->map_out = out;
+  h->map_n = n;
+  return NM_OK;
+}
+
+PackParams make_pack_params(const nm_mlp* h) {
+  PackParams pp;
+  std::memset(&pp, 0, sizeof(pp));
+  pp.L = h->L;
+  uint32_t cw = 0, cb = 0;
+  for (int l = 0; l <= h->L; ++l) pp.dims[l] = h->dims[l];
+  for (int l = 0; l < h->L; ++l) {
+    pp.w_off[l] = h->params.w_off[l];
+    pp.chunk_start[l] = cw;
+    pp.bias_chunk_start[l] = cb;
+    cw += static_cast<uint32_t>(h->dims[l] * h->dims[l + 1] / 8);
+    cb += static_cast<uint32_t>(h->dims[l + 1] / 8);
+  }
+  pp.chunk_start[h->L] = cw;
+  pp.bias_chunk_start[h->L] = cb;
+  pp.bias_off = h->params.bias_off;
+  pp.blob = h->blob;
+  return pp;
+}
+
+nm_status ensure_mirror(nm_mlp* h, cudaStream_t stream) {
+  if (h->mirror_valid) return NM_OK;
+  if (!h->mirror) {
+    if (cudaMalloc(&h->mirror, h->mirror_elems * sizeof(uint16_t)) != cudaSuccess) {
+      h->mirror = nullptr;
+      return NM_ERR_OOM;
+    }
+  }
+  PackParams pp = make_pack_params(h);
+  for (int l = 0; l < h->L; ++l) {
+    pp.rm_w[l] = h->mirror + h->params.rm_off[l];
+    pp.rm_b[l] = h->mirror + h->rm_b_off[l];
+  }
+  if (nm::launch_pack(pp, true, h->num_sms, stream) != cudaSuccess) return NM_ERR_CUDA;
+  h->params.mirror = h->mirror;
+  h->mirror_valid = true;
+  return NM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t nm_abi_version(void) { return 1; }
+
+const char* nm_status_str(nm_status s) {
+  switch (s) {
+    case NM_OK: return "NM_OK";
+    case NM_ERR_INVALID_ARG: return "NM_ERR_INVALID_ARG";
+    case NM_ERR_UNSUPPORTED: return "NM_ERR_UNSUPPORTED";
+    case NM_ERR_NOT_PACKED: return "NM_ERR_NOT_PACKED";
+    case NM_ERR_OOM: return "NM_ERR_OOM";
+    case NM_ERR_CUDA: return "NM_ERR_CUDA";
+    case NM_ERR_TIMEOUT: return "NM_ERR_TIMEOUT";
+  }
+  return "NM_ERR_UNKNOWN";
+}
+
+nm_status nm_mlp_create(const int32_t* dims, int32_t n_dims, nm_mlp** out) {
+  if (!out) return NM_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!dims || n_dims < 2) return NM_ERR_INVALID_ARG;
+  const int L = n_dims - 1;
+  if (L > nm::kMaxLayers) return NM_ERR_UNSUPPORTED;
+  for (int l = 0; l <= L; ++l)
+    if (dims[l] < 16 || dims[l] > nm::kMaxDim || dims[l] % 16 != 0) return NM_ERR_UNSUPPORTED;
+
+  int dev = 0, major = 0, minor = 0, sms = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NM_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return NM_ERR_CUDA;
+  if (major != 10 || minor != 3) return NM_ERR_UNSUPPORTED;
+
+  nm_mlp* h = new (std::nothrow) nm_mlp();
+  if (!h) return NM_ERR_OOM;
+  h->L = L;
+  h->device = dev;
+  h->num_sms = sms;
+  h->smem_optin = static_cast<uint32_t>(optin);
+  FusedParams& p = h->params;
+  std::memset(&p, 0, sizeof(p));
+  p.L = L;
+  uint32_t off = 0;
+  size_t rm = 0;
+  for (int l = 0; l <= L; ++l) h->dims[l] = p.dims[l] = dims[l];
+  for (int l = 0; l < L; ++l) {
+    off = nm::align1024(off);
+    p.w_off[l] = off;
+    off += nm::image_bytes(static_cast<uint32_t>(dims[l + 1]), dims[l]);
+    p.rm_off[l] = static_cast<uint32_t>(rm);
+    rm += static_cast<size_t>(dims[l]) * dims[l + 1];
+  }
+  for (int l = 0; l < L; ++l) {
+    h->rm_b_off[l] = static_cast<uint32_t>(rm);
+    rm += static_cast<size_t>(dims[l + 1]);
+  }
+  h->mirror_elems = rm;
+  p.bias_off = nm::align1024(off);
+  uint32_t nb = 0;
+  for (int l = 0; l < L; ++l) nb += static_cast<uint32_t>(dims[l + 1]);
+  h->blob_size = p.bias_off + 2u * nb;
+
+  if (cudaMalloc(&h->blob, h->blob_size) != cudaSuccess) {
+    delete h;
+    return NM_ERR_OOM;
+  }
+  if (cudaMalloc(&h->status, sizeof(uint32_t)) != cudaSuccess) {
+    cudaFree(h->blob);
+    delete h;
+    return NM_ERR_OOM;
+  }
+  if (cudaMemset(h->blob, 0, h->blob_size) != cudaSuccess ||
+      cudaMemset(h->status, 0, sizeof(uint32_t)) != cudaSuccess) {
+    cudaFree(h->blob);
+    cudaFree(h->status);
+    delete h;
+    return NM_ERR_CUDA;
+  }
+  p.blob = h->blob;
+  p.status = h->status;
+  *out = h;
+  return NM_OK;
+}
+
+nm_status nm_mlp_packed_size(const nm_mlp* h, size_t* bytes) {
+  if (!h || !bytes) return NM_ERR_INVALID_ARG;
+  *bytes = h->blob_size;
+  return NM_OK;
+}
+
+nm_status nm_mlp_packed_blob(const nm_mlp* h, const void** blob) {
+  if (!h || !blob) return NM_ERR_INVALID_ARG;
+  *blob = h->blob;
+  return NM_OK;
+}
+
+nm_status nm_mlp_pack_weights(nm_mlp* h, const void* const* W, const void* const* b,
+                              nm_stream stream) {
+  if (!h || !W || !b) return NM_ERR_INVALID_ARG;
+  PackParams pp = make_pack_params(h);
+  for (int l = 0; l < h->L; ++l) {
+    if (!W[l] || !b[l] || !aligned16(W[l]) || !aligned16(b[l])) return NM_ERR_INVALID_ARG;
+    pp.rm_w[l] = const_cast<uint16_t*>(static_cast<const uint16_t*>(W[l]));
+    pp.rm_b[l] = const_cast<uint16_t*>(static_cast<const uint16_t*>(b[l]));
+  }
+  if (nm::launch_pack(pp, false, h->num_sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return NM_ERR_CUDA;
+  h->packed = true;
+  h->mirror_valid = false;
+  return NM_OK;
+}
+
+nm_status nm_mlp_unpack_weights(const nm_mlp* h, void* const* W, void* const* b, nm_stream stream) {
+  if (!h || !W || !b) return NM_ERR_INVALID_ARG;
+  if (!h->packed) return NM_ERR_NOT_PACKED;
+  PackParams pp = make_pack_params(h);
+  for (int l = 0; l < h->L; ++l) {
+    if (!W[l] || !b[l] || !aligned16(W[l]) || !aligned16(b[l])) return NM_ERR_INVALID_ARG;
+    pp.rm_w[l] = static_cast<uint16_t*>(W[l]);
+    pp.rm_b[l] = static_cast<uint16_t*>(b[l]);
+  }
+  if (nm::launch_pack(pp, true, h->num_sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return NM_ERR_CUDA;
+  return NM_OK;
+}
+
+nm_status nm_mlp_infer(nm_mlp* h, const void* in, int64_t n, void* out, nm_stream stream) {
+  if (!h) return NM_ERR_INVALID_ARG;
+  if (n < 0 || n > (static_cast<int64_t>(1) << 31) - 128) return NM_ERR_INVALID_ARG;
+  if (n == 0) return NM_OK;
+  if (!in || !out || !aligned16(in) || !aligned16(out)) return NM_ERR_INVALID_ARG;
+  if (!h->packed) return NM_ERR_NOT_PACKED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (h->variant == nm::kVarRowMajor) {
+    const nm_status st = ensure_mirror(h, s);
+    if (st != NM_OK) return st;
+  }
+  nm_status st = encode_io_maps(h, in, out, n);
+  if (st != NM_OK) return st;
+  FusedParams& p = h->params;
+  p.n = n;
+  p.num_tiles = static_cast<int32_t>((n + nm::kTileM - 1) / nm::kTileM);
+  p.wait_ns = h->wait_ns;
+  const uint32_t smem = nm::plan_fused_smem(p, h->variant, h->smem_optin);
+  if (smem == 0) return NM_ERR_UNSUPPORTED;
+  const int grid = p.num_tiles < h->num_sms ? p.num_tiles : h->num_sms;
+  if (nm::launch_fused(p, h->variant, grid, smem, s) != cudaSuccess) return NM_ERR_CUDA;
+  return NM_OK;
+}
+
+nm_status nm_mlp_set_variant(nm_mlp* h, nm_variant v) {
+  if (!h) return NM_ERR_INVALID_ARG;
+  if (v != NM_VARIANT_FUSED && v != NM_VARIANT_ROWMAJOR_WEIGHTS && v != NM_VARIANT_SCALAR_ACTIVATION)
+    return NM_ERR_INVALID_ARG;
+  h->variant = static_cast<int>(v);
+  return NM_OK;
+}
+
+nm_status nm_mlp_device_status(nm_mlp* h, nm_stream stream) {
+  if (!h) return NM_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return NM_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, h->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return NM_ERR_CUDA;
+  if (v != 0) {
+    if (cudaMemset(h->status, 0, sizeof(uint32_t)) != cudaSuccess) return NM_ERR_CUDA;
+    return NM_ERR_TIMEOUT;
+  }
+  return NM_OK;
+}
+
+nm_status nm_mlp_set_wait_limit(nm_mlp* h, uint64_t nanoseconds) {
+  if (!h) return NM_ERR_INVALID_ARG;
+  h->wait_ns = nanoseconds;
+  return NM_OK;
+}
+
+void nm_mlp_destroy(nm_mlp* h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  cudaFree(h->blob);
+  cudaFree(h->status);
+  if (h->mirror) cudaFree(h->mirror);
+  delete h;
+}
+
+}  // extern "C"

@@ -1,0 +1,171 @@
+"""Thin ctypes binding of libnmmlp (include/nm_mlp.h): same names, argument
+marshalling only. Every step of inference runs in the library's CUDA
+kernels; there is no other implementation behind these calls, and a missing
+library raises instead of falling back.
+
+Tensors are PyTorch CUDA tensors (used for device memory and streams only);
+raw device addresses (ints) are accepted wherever a tensor is.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+NM_OK = 0
+NM_ERR_INVALID_ARG = 1
+NM_ERR_UNSUPPORTED = 2
+NM_ERR_NOT_PACKED = 3
+NM_ERR_OOM = 4
+NM_ERR_CUDA = 5
+NM_ERR_TIMEOUT = 6
+
+NM_VARIANT_FUSED = 0
+NM_VARIANT_ROWMAJOR_WEIGHTS = 1
+NM_VARIANT_SCALAR_ACTIVATION = 2
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnmmlp.so")
+
+# Every symbol include/nm_mlp.h declares, with (restype, argtypes).
+_P = ctypes.c_void_p
+SIGNATURES = {
+    "nm_abi_version": (ctypes.c_int32, []),
+    "nm_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+    "nm_mlp_create": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(_P)]),
+    "nm_mlp_packed_size": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_size_t)]),
+    "nm_mlp_pack_weights": (ctypes.c_int, [_P, _P, _P, _P]),
+    "nm_mlp_unpack_weights": (ctypes.c_int, [_P, _P, _P, _P]),
+    "nm_mlp_packed_blob": (ctypes.c_int, [_P, ctypes.POINTER(_P)]),
+    "nm_mlp_infer": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P, _P]),
+    "nm_mlp_set_variant": (ctypes.c_int, [_P, ctypes.c_int]),
+    "nm_mlp_device_status": (ctypes.c_int, [_P, _P]),
+    "nm_mlp_set_wait_limit": (ctypes.c_int, [_P, ctypes.c_uint64]),
+    "nm_mlp_destroy": (None, [_P]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class NmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_str(status)} ({status})")
+
+
+def lib():
+    """Open libnmmlp.so (built by __graft_entry__.build() or
+    ``python -m mlp_neural_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m mlp_neural_gb300.build` (there is no fallback path)")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+        return _lib
+
+
+def status_str(status: int) -> str:
+    return lib().nm_status_str(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != NM_OK:
+        raise NmError(status, what)
+
+
+def _addr(t) -> int:
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    return int(t.data_ptr())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+class MLP:
+    """Owns one nm_mlp handle (dims, packed weights on the device)."""
+
+    def __init__(self, dims):
+        self.dims = [int(d) for d in dims]
+        arr = (ctypes.c_int32 * len(self.dims))(*self.dims)
+        h = ctypes.c_void_p()
+        _check(lib().nm_mlp_create(arr, len(self.dims), ctypes.byref(h)), "nm_mlp_create")
+        self._h = h
+
+    @property
+    def handle(self) -> int:
+        return self._h.value
+
+    @property
+    def n_layers(self) -> int:
+        return len(self.dims) - 1
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().nm_mlp_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def packed_size(self) -> int:
+        n = ctypes.c_size_t()
+        _check(lib().nm_mlp_packed_size(self._h, ctypes.byref(n)), "nm_mlp_packed_size")
+        return n.value
+
+    def packed_blob(self) -> int:
+        p = ctypes.c_void_p()
+        _check(lib().nm_mlp_packed_blob(self._h, ctypes.byref(p)), "nm_mlp_packed_blob")
+        return p.value
+
+    def pack_weights(self, W, b, stream=None):
+        Wp = (ctypes.c_void_p * len(W))(*[_addr(w) for w in W])
+        bp = (ctypes.c_void_p * len(b))(*[_addr(v) for v in b])
+        _check(lib().nm_mlp_pack_weights(self._h, Wp, bp, _stream(stream)), "nm_mlp_pack_weights")
+
+    def unpack_weights(self, W, b, stream=None):
+        Wp = (ctypes.c_void_p * len(W))(*[_addr(w) for w in W])
+        bp = (ctypes.c_void_p * len(b))(*[_addr(v) for v in b])
+        _check(lib().nm_mlp_unpack_weights(self._h, Wp, bp, _stream(stream)),
+               "nm_mlp_unpack_weights")
+
+    def infer_raw(self, in_ptr: int, n: int, out_ptr: int, stream=None) -> int:
+        """nm_mlp_infer on raw addresses; returns the status code."""
+        return lib().nm_mlp_infer(self._h, in_ptr, int(n), out_ptr, _stream(stream))
+
+    def infer(self, x, out=None, stream=None):
+        """out[n, d_L] = network(x[n, d_0]); both FP16 CUDA tensors."""
+        import torch
+        n = x.shape[0]
+        if out is None:
+            out = torch.empty((n, self.dims[-1]), dtype=torch.float16, device=x.device)
+        _check(self.infer_raw(_addr(x), n, _addr(out), stream), "nm_mlp_infer")
+        return out
+
+    def set_variant(self, v: int):
+        _check(lib().nm_mlp_set_variant(self._h, int(v)), "nm_mlp_set_variant")
+
+    def device_status(self, stream=None) -> int:
+        return lib().nm_mlp_device_status(self._h, _stream(stream))
+
+    def set_wait_limit(self, ns: int):
+        _check(lib().nm_mlp_set_wait_limit(self._h, int(ns)), "nm_mlp_set_wait_limit")

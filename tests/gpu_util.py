@@ -1,0 +1,80 @@
+"""Helpers for the GPU tests: build/load the library, move uint16 FP16 bits
+between numpy and torch CUDA tensors, read raw device memory, run the oracle.
+"""
+import ctypes
+import glob
+import os
+
+import numpy as np
+
+TOL_ABS = 1e-2
+TOL_REL = 1e-2
+
+
+def nm():
+    from mlp_neural_gb300 import build, nm as _nm
+    build.build()
+    return _nm
+
+
+def to_dev(a16: np.ndarray):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a16).view(np.int16)).cuda().view(torch.float16)
+
+
+def to_host(t) -> np.ndarray:
+    import torch
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+_cudart = None
+
+
+def _rt():
+    global _cudart
+    if _cudart is None:
+        import torch
+        cands = glob.glob(os.path.join(os.path.dirname(torch.__file__), "..", "nvidia", "*", "lib",
+                                       "libcudart.so*"))
+        cands += ["libcudart.so.13", "/usr/local/cuda/lib64/libcudart.so"]
+        for c in cands:
+            try:
+                _cudart = ctypes.CDLL(c)
+                break
+            except OSError:
+                continue
+        _cudart.cudaMemcpy.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
+    return _cudart
+
+
+def read_device(ptr: int, nbytes: int) -> np.ndarray:
+    import torch
+    torch.cuda.synchronize()
+    out = np.empty(nbytes, np.uint8)
+    rc = _rt().cudaMemcpy(out.ctypes.data, ptr, nbytes, 2)  # cudaMemcpyDeviceToHost
+    assert rc == 0, rc
+    return out
+
+
+def make_net(dims, W, b):
+    """Create a library handle and pack W/b (uint16 numpy) into it."""
+    lib = nm()
+    m = lib.MLP(dims)
+    Wd = [to_dev(w) for w in W]
+    bd = [to_dev(v) for v in b]
+    m.pack_weights(Wd, bd)
+    import torch
+    torch.cuda.synchronize()
+    return m
+
+
+def assert_close(gpu16: np.ndarray, cpu16: np.ndarray, what=""):
+    g = gpu16.view(np.float16).astype(np.float64)
+    c = cpu16.view(np.float16).astype(np.float64)
+    assert g.shape == c.shape, (g.shape, c.shape)
+    err = np.abs(g - c)
+    bound = TOL_ABS + TOL_REL * np.abs(c)
+    bad = np.argwhere(~(err <= bound))
+    assert bad.size == 0, (f"{what}: {len(bad)} elements outside |gpu-cpu| <= 1e-2 + 1e-2|cpu|; "
+                           f"first {bad[:5].tolist()} gpu={g[tuple(bad[0])]} cpu={c[tuple(bad[0])]}")
+    return float(err.max()) if err.size else 0.0
