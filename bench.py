@@ -1,0 +1,402 @@
+#!/usr/bin/env python
+"""Benchmark: batched inference of the fused FP16 MLP on GB300.
+
+One step = one dispatch of the whole hot path (every layer of the network on
+every input of the workload) through the C ABI (nm_mlp_infer). Default
+workload: the page-shaped network 48 -> 64x7 -> 16 on 65,536 fixed inputs
+evaluated 16 times = 1,048,576 evaluations per dispatch ("Profiling neural
+material inference", "Experiment setup").
+
+Prints one JSON line (rank 0). `--impl reference` times the CPU oracle
+instead, on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "M network evals/sec (fused FP16 MLP, 1 GB300); % of FP16 tensor-core roofline"
+UNIT = "M evals/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CLOCK_FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+VARIANTS = {"fused": 0, "rowmajor": 1, "scalar": 2}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for about a second of GPU time)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="page")
+    ap.add_argument("--variant", choices=tuple(VARIANTS), default="fused")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def default_steps(w) -> int:
+    # about 1 s of GPU work at ~30 G evals/s, so the clock sampler sees the run
+    return max(200, int(3.0e10 / w.n_evals))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mlp_neural_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def load_traffic(workload: str, variant: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"fused_mlp_{variant}_{workload}.traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_sources_sha256") != kernel_sources_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def roofline_bound(w, peaks):
+    t_tensor = w.flops_per_eval / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = w.hbm_bytes_per_eval / (peaks["hbm_gbs"] * 1e9)
+    return ("tensor" if t_tensor >= t_hbm else "hbm"), t_tensor, t_hbm
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    def __init__(self, device_index):
+        self.proc = None
+        self.lines = []
+        cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        if device_index is not None:
+            cmd += ["-i", str(device_index)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self, t0, t1):
+        import datetime
+        samples = []
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                samples.append((ts, float(parts[1]), float(parts[2]), parts[3], parts[4:]))
+            except ValueError:
+                continue
+        inside = [s for s in samples if t0 - 0.05 <= s[0] <= t1 + 0.05]
+        used = inside if inside else samples
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        mhz = sorted(s[1] for s in used)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for s in used:
+            for name, val in zip(names, s[4][1:]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(s[2] for s in used),
+                "reasons": sorted(reasons), "samples": len(inside),
+                "window": "timed region" if inside else "whole run (no sample fell inside)"}
+
+
+def _nvsmi_index(dev):
+    import torch
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid).replace("GPU-", "")
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            return vis.split(",")[dev]
+        return dev
+
+
+# ---------------------------------------------------------------- oracle (CPU)
+def _oracle_sample(w, n_evals: int):
+    """Weights, biases and the first n_evals rows of one dispatch (the unique
+    inputs, repeated as the dispatch repeats them)."""
+    import numpy as np
+    from mlp_neural_gb300 import synth
+    W, b = synth.net_params(w.dims, w.seed)
+    nu = min(n_evals, w.n_unique)
+    x = synth.inputs(w, 0, nu)
+    x = np.concatenate([x] * math.ceil(n_evals / nu))[:n_evals]
+    return W, b, np.ascontiguousarray(x)
+
+
+def oracle_rate(w, n_evals: int):
+    """Time the oracle, as it stands, on the first n_evals rows of a dispatch."""
+    import oracle
+    oracle.build()
+    W, b, x = _oracle_sample(w, n_evals)
+    t0 = time.perf_counter()
+    oracle.forward(w.dims, W, b, x)
+    dt = time.perf_counter() - t0
+    return n_evals / dt / 1e6, dt
+
+
+def run_reference(args, w, rank):
+    """The reference arm: the CPU oracle on this host, one bounded sample of
+    the workload per step, sized so the whole run takes about two minutes."""
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    K, W = args.steps if args.steps is not None else default_steps(w), args.warmup
+    _, dt = oracle_rate(w, 256)
+    per_eval = dt / 256
+    per_step = int(max(16, min(65536, 120.0 / (per_eval * max(1, K + W)))))
+    Wt, bt, x = _oracle_sample(w, per_step)
+    for _ in range(W):
+        oracle.forward(w.dims, Wt, bt, x)
+    t_total = 0.0
+    for _ in range(K):
+        t0 = time.perf_counter()
+        oracle.forward(w.dims, Wt, bt, x)
+        t_total += time.perf_counter() - t0
+    value = per_step * K / t_total / 1e6
+    sample = (f"{per_step} of the {w.n_evals:,} evaluations of one dispatch per step "
+              f"(first rows), single thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": K, "warmup": W, "ms_per_step": t_total / K * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": w.name, "dims": list(w.dims), "evals_per_step": w.n_evals,
+            "unique_inputs": w.n_unique, "repeats": w.repeats, "seed": w.seed,
+            "inputs": w.input_dist}
+
+
+# ---------------------------------------------------------------- GPU arm
+def main(argv=None):
+    args = parse_args(argv)
+    from mlp_neural_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, w, rank)
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from mlp_neural_gb300 import build as nm_build
+    from mlp_neural_gb300 import nm
+
+    K = args.steps if args.steps is not None else default_steps(w)
+    Wu = args.warmup
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    nm_build.build()
+    stream = torch.cuda.current_stream(dev)
+
+    # network + one-time weight conversion (timed on its own, like the page's
+    # conversion cost, and excluded from the steady state)
+    Wt, bt = synth.net_params(w.dims, w.seed)
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.float16)
+    Wd, bd = [to_dev(x) for x in Wt], [to_dev(x) for x in bt]
+    m = nm.MLP(w.dims)
+    m.set_variant(VARIANTS[args.variant])
+    m.pack_weights(Wd, bd, stream)
+    torch.cuda.synchronize()
+    pe0, pe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pack_ms = []
+    for _ in range(5):
+        pe0.record(stream)
+        m.pack_weights(Wd, bd, stream)
+        pe1.record(stream)
+        torch.cuda.synchronize()
+        pack_ms.append(pe0.elapsed_time(pe1))
+    pack_ms = sorted(pack_ms)[len(pack_ms) // 2]
+
+    # inputs: this rank's unique rows, repeated as the dispatch repeats them
+    xu = synth.inputs(w, rank * w.n_unique, w.n_unique)
+    xdev = to_dev(xu)
+    if w.repeats > 1:
+        xdev = xdev.repeat(w.repeats, 1)
+    n = xdev.shape[0]
+    d_out = w.dims[-1]
+    set_bytes = n * 2 * (w.dims[0] + d_out)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nsets = max(1, math.ceil(2 * l2 / set_bytes) + 1) if set_bytes < 2 * l2 else 1
+    ins = [xdev] + [xdev.clone() for _ in range(nsets - 1)]
+    outs = [torch.empty((n, d_out), dtype=torch.float16, device=dev) for _ in range(nsets)]
+    l2_note = (f"rotating {nsets} input/output buffer sets ({nsets * set_bytes / 1e6:.0f} MB > 2x L2 "
+               f"{l2 / 1e6:.0f} MB)" if nsets > 1 else
+               f"inputs+outputs {set_bytes / 1e6:.0f} MB per step > 2x L2")
+
+    def launch(i):
+        st = m.infer_raw(ins[i % nsets].data_ptr(), n, outs[i % nsets].data_ptr(), stream)
+        if st != nm.NM_OK:
+            raise nm.NmError(st, "nm_mlp_infer")
+
+    for i in range(Wu):
+        launch(i)
+    torch.cuda.synchronize()
+    if m.device_status(stream) != nm.NM_OK:
+        raise RuntimeError("device status after warm-up")
+
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(_nvsmi_index(local)) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(K):
+        ev0[i].record(stream)
+        launch(i)
+        ev1[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        dist.barrier()
+    time.sleep(0.15 if sampler else 0)
+    if sampler:
+        sampler.stop()
+    if m.device_status(stream) != nm.NM_OK:
+        raise RuntimeError("device status after the timed region")
+    total_ms = ev0[0].elapsed_time(ev1[K - 1])
+    kernel_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(K)]
+    avg_kernel_ms = sum(kernel_ms) / K
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    evals_all = w.n_evals * K * world
+    value = evals_all / (total_ms * 1e-3) / 1e6
+
+    # end to end through the C ABI from pinned host memory: H2D copy of the
+    # step's inputs, the dispatch, D2H copy of the step's outputs
+    hin = torch.empty((n, w.dims[0]), dtype=torch.float16, pin_memory=True)
+    hin.copy_(xdev.cpu())
+    hout = torch.empty((n, d_out), dtype=torch.float16, pin_memory=True)
+    E = args.e2e_steps
+
+    def e2e_step():
+        ins[0].copy_(hin, non_blocking=True)
+        launch(0)
+        hout.copy_(outs[0], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    if world > 1:
+        dist.barrier()
+    te0 = time.perf_counter()
+    for _ in range(E):
+        e2e_step()
+    te = time.perf_counter() - te0
+    if world > 1:
+        t = torch.tensor([te], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        te = float(t.item())
+    e2e_value = w.n_evals * E * world / te / 1e6
+
+    peaks, peaks_src = load_peaks()
+    bound, _, _ = roofline_bound(w, peaks)
+    if bound == "tensor":
+        achieved = w.flops_per_eval * n / (avg_kernel_ms * 1e-3) / 1e12
+        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved = w.hbm_bytes_per_eval * n / (avg_kernel_ms * 1e-3) / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": load_traffic(w.name, args.variant),
+                "kernel": "fused_mlp_kernel", "peak_source": (
+                    f"{peaks_src}: " + ("dense bf16 burst (FP16 dense has the same nominal rate)"
+                                        if bound == "tensor" else "HBM copy bandwidth"))}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": Wu, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": dict(workload_config(w), variant=args.variant, l2=l2_note,
+                       parallelism=f"replicas x{world}, no collective on the data path"),
+        "roofline": roofline,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(hin.numel() * 2),
+                "d2h_bytes_per_step": int(hout.numel() * 2)},
+        "gpu_launches": K,
+        "kernel_ms": avg_kernel_ms,
+        "pack_ms": pack_ms,
+    }
+    if sampler:
+        line["clocks"] = sampler.summary(t0, t1)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample_n = min(131072, w.n_evals)
+        v, dt = oracle_rate(w, sample_n)
+        line["cpu_baseline"] = {
+            "value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {sample_n:,} of the {w.n_evals:,} evaluations of one dispatch, "
+                      f"single thread, {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    m.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

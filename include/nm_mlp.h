@@ -131,7 +131,7 @@ nm_status nm_mlp_packed_blob(const nm_mlp *h, const void **blob);
 /* Evaluate the network on n inputs ("Experiment setup": one dispatch).
  * in:  device FP16 [n][dims[0]] row-major.   out: device FP16 [n][dims[L]].
  * n == 0 is a no-op. Rows of `out` beyond n are never written.
- * Errors: NM_ERR_INVALID_ARG (NULL/misaligned pointers, n < 0 or n >= 2^38),
+ * Errors: NM_ERR_INVALID_ARG (NULL/misaligned pointers, n < 0 or n > 2^31 - 128),
  * NM_ERR_NOT_PACKED, NM_ERR_UNSUPPORTED (the network does not fit the
  * selected variant's shared-memory budget), NM_ERR_CUDA (launch failure).
  * A kernel-side wait that gives up is reported by nm_mlp_device_status. */
@@ -152,6 +152,13 @@ nm_status nm_mlp_device_status(nm_mlp *h, nm_stream stream);
  * the kernel winds down (drains its copies in flight, frees its tensor
  * memory) and returns. Tests set a tiny limit to exercise that path. */
 nm_status nm_mlp_set_wait_limit(nm_mlp *h, uint64_t nanoseconds);
+
+/* Test hook for the failure path. With `enable` non-zero, every CTA of later
+ * nm_mlp_infer launches first waits on a barrier that nothing ever signals,
+ * so that wait runs out after the wait limit: the kernel then takes its
+ * give-up path (status word set, copies drained, tensor memory freed) without
+ * any fault. The outputs of such a launch are undefined. */
+nm_status nm_mlp_set_test_stall(nm_mlp *h, int32_t enable);
 
 /* Free the handle and its device memory (synchronises the device first).
  * NULL is a no-op. */

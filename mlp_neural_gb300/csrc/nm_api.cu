@@ -86,6 +86,7 @@ struct nm_mlp {
   bool mirror_valid = false;
   int variant = nm::kVarFused;
   uint64_t wait_ns = 2000000000ull;
+  uint32_t test_stall = 0;
   int device = 0;
   int num_sms = 0;
   uint32_t smem_optin = 0;
@@ -340,6 +341,7 @@ nm_status nm_mlp_infer(nm_mlp* h, const void* in, int64_t n, void* out, nm_strea
   p.n = n;
   p.num_tiles = static_cast<int32_t>((n + nm::kTileM - 1) / nm::kTileM);
   p.wait_ns = h->wait_ns;
+  p.test_stall = h->test_stall;
   const uint32_t smem = nm::plan_fused_smem(p, h->variant, h->smem_optin);
   if (smem == 0) return NM_ERR_UNSUPPORTED;
   const int grid = p.num_tiles < h->num_sms ? p.num_tiles : h->num_sms;
@@ -370,6 +372,12 @@ nm_status nm_mlp_device_status(nm_mlp* h, nm_stream stream) {
 nm_status nm_mlp_set_wait_limit(nm_mlp* h, uint64_t nanoseconds) {
   if (!h) return NM_ERR_INVALID_ARG;
   h->wait_ns = nanoseconds;
+  return NM_OK;
+}
+
+nm_status nm_mlp_set_test_stall(nm_mlp* h, int32_t enable) {
+  if (!h) return NM_ERR_INVALID_ARG;
+  h->test_stall = enable ? 1u : 0u;
   return NM_OK;
 }
 

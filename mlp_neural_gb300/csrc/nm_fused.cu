@@ -193,7 +193,9 @@ __device__ __forceinline__ void run_mma(const FusedParams& p, const Ctx& c) {
   const uint32_t R = p.n_in_stages;
   const int L = p.L;
   bool ok = true;
-  if (V != kVarRowMajor) ok = wait_phase(c.bar(kBarWLoad), 0, p.wait_ns, c.abort_flag, p.status);
+  if (p.test_stall) ok = wait_phase(c.bar(kBarNever), 0, p.wait_ns, c.abort_flag, p.status);
+  if (ok && V != kVarRowMajor)
+    ok = wait_phase(c.bar(kBarWLoad), 0, p.wait_ns, c.abort_flag, p.status);
   uint32_t i = 0, g = 0;
   for (int32_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++i) {
     const uint32_t s = i & 1u, st = i % R, rnd = i / R;
@@ -365,6 +367,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
     mbar_init(c.bar(kBarWLoad), 1);
     mbar_init(c.bar(kBarDrain), 1);
+    mbar_init(c.bar(kBarNever), 1);
     *c.abort_flag = 0u;
     fence_mbar_init();
   }

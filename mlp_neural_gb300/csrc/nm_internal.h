@@ -28,7 +28,8 @@ enum BarIndex : int {
   kBarBEmpty = kBarBFull + kMaxBStages,
   kBarWLoad = kBarBEmpty + kMaxBStages,
   kBarDrain = kBarWLoad + 1,
-  kBarCount = kBarDrain + 1
+  kBarNever = kBarDrain + 1,  // never signalled (failure-path test hook)
+  kBarCount = kBarNever + 1
 };
 constexpr uint32_t kBarBlockBytes = 256;  // kBarCount * 8 barriers, then TMEM address and abort flag
 constexpr uint32_t kTmemSlotOff = 192;
@@ -57,6 +58,7 @@ struct FusedParams {  // 128-byte aligned through its CUtensorMap members
   uint32_t tmem_cols;  // allocated TMEM columns (power of two)
   uint32_t nmax;       // TMEM columns per tile slot (max layer width)
   uint64_t wait_ns;    // limit of every pipeline wait
+  uint32_t test_stall; // non-zero: the MMA thread first waits on kBarNever
 };
 
 // Returns the dynamic smem bytes the plan needs, or 0 if it does not fit.

@@ -40,6 +40,7 @@ SIGNATURES = {
     "nm_mlp_set_variant": (ctypes.c_int, [_P, ctypes.c_int]),
     "nm_mlp_device_status": (ctypes.c_int, [_P, _P]),
     "nm_mlp_set_wait_limit": (ctypes.c_int, [_P, ctypes.c_uint64]),
+    "nm_mlp_set_test_stall": (ctypes.c_int, [_P, ctypes.c_int32]),
     "nm_mlp_destroy": (None, [_P]),
 }
 
@@ -169,3 +170,6 @@ class MLP:
 
     def set_wait_limit(self, ns: int):
         _check(lib().nm_mlp_set_wait_limit(self._h, int(ns)), "nm_mlp_set_wait_limit")
+
+    def set_test_stall(self, enable: bool):
+        _check(lib().nm_mlp_set_test_stall(self._h, 1 if enable else 0), "nm_mlp_set_test_stall")
