@@ -73,11 +73,14 @@ using nm::FusedParams;
 using nm::PackParams;
 
 struct nm_mlp {
-  FusedParams params;  // kernel parameter block (dims, offsets, tensor maps)
+  FusedParams params;  // kernel parameter block (offsets, tensor maps, plan)
   int L = 0;
   int32_t dims[nm::kMaxLayers + 1] = {};
+  uint32_t w_off[nm::kMaxLayers] = {};   // byte offset of each layer's image in the blob
+  uint32_t rm_off[nm::kMaxLayers] = {};  // element offset of each W_l in the mirror
   size_t blob_size = 0;
   uint8_t* blob = nullptr;       // packed weight images + FP16 biases (device)
+  uint8_t* sched = nullptr;      // nm::Schedule (device)
   uint32_t* status = nullptr;    // device status word
   uint16_t* mirror = nullptr;    // row-major weights + biases for the row-major ablation
   uint32_t rm_b_off[nm::kMaxLayers] = {};
@@ -144,9 +147,15 @@ nm_status encode_io_maps(nm_mlp* h, const void* in, void* out, int64_t n) {
     st = encode_map(&p.tm_in[nm::swizzle_kind(w[s])], in, h->dims[0], n, w[s], nm::kTileM);
     if (st != NM_OK) return st;
   }
-  ns = nm::segments(h->dims[h->L], w, k0);
-  for (int s = 0; s < ns; ++s) {
-    st = encode_map(&p.tm_out[nm::swizzle_kind(w[s])], out, h->dims[h->L], n, w[s], 32);
+  // Output: 32-row boxes of 32 columns (64-byte swizzle), plus 16 columns
+  // (32-byte swizzle) for a trailing 16-column chunk.
+  const int dl = h->dims[h->L];
+  if (dl >= 32) {
+    st = encode_map(&p.tm_out[nm::swizzle_kind(32)], out, dl, n, 32, 32);
+    if (st != NM_OK) return st;
+  }
+  if (dl & 31) {
+    st = encode_map(&p.tm_out[nm::swizzle_kind(16)], out, dl, n, 16, 32);
     if (st != NM_OK) return st;
   }
   h->map_in = in;
@@ -162,7 +171,7 @@ PackParams make_pack_params(const nm_mlp* h) {
   uint32_t cw = 0, cb = 0;
   for (int l = 0; l <= h->L; ++l) pp.dims[l] = h->dims[l];
   for (int l = 0; l < h->L; ++l) {
-    pp.w_off[l] = h->params.w_off[l];
+    pp.w_off[l] = h->w_off[l];
     pp.chunk_start[l] = cw;
     pp.bias_chunk_start[l] = cb;
     cw += static_cast<uint32_t>(h->dims[l] * h->dims[l + 1] / 8);
@@ -185,7 +194,7 @@ nm_status ensure_mirror(nm_mlp* h, cudaStream_t stream) {
   }
   PackParams pp = make_pack_params(h);
   for (int l = 0; l < h->L; ++l) {
-    pp.rm_w[l] = h->mirror + h->params.rm_off[l];
+    pp.rm_w[l] = h->mirror + h->rm_off[l];
     pp.rm_b[l] = h->mirror + h->rm_b_off[l];
   }
   if (nm::launch_pack(pp, true, h->num_sms, stream) != cudaSuccess) return NM_ERR_CUDA;
@@ -242,12 +251,12 @@ nm_status nm_mlp_create(const int32_t* dims, int32_t n_dims, nm_mlp** out) {
   p.L = L;
   uint32_t off = 0;
   size_t rm = 0;
-  for (int l = 0; l <= L; ++l) h->dims[l] = p.dims[l] = dims[l];
+  for (int l = 0; l <= L; ++l) h->dims[l] = dims[l];
   for (int l = 0; l < L; ++l) {
     off = nm::align1024(off);
-    p.w_off[l] = off;
+    h->w_off[l] = off;
     off += nm::image_bytes(static_cast<uint32_t>(dims[l + 1]), dims[l]);
-    p.rm_off[l] = static_cast<uint32_t>(rm);
+    h->rm_off[l] = static_cast<uint32_t>(rm);
     rm += static_cast<size_t>(dims[l]) * dims[l + 1];
   }
   for (int l = 0; l < L; ++l) {
@@ -260,22 +269,38 @@ nm_status nm_mlp_create(const int32_t* dims, int32_t n_dims, nm_mlp** out) {
   for (int l = 0; l < L; ++l) nb += static_cast<uint32_t>(dims[l + 1]);
   h->blob_size = p.bias_off + 2u * nb;
 
+  nm::Schedule* sc = new (std::nothrow) nm::Schedule;
+  if (!sc) {
+    delete h;
+    return NM_ERR_OOM;
+  }
+  p.sched_bytes = nm::build_schedule(h->dims, L, h->w_off, h->rm_off, *sc);
+
   if (cudaMalloc(&h->blob, h->blob_size) != cudaSuccess) {
+    delete sc;
     delete h;
     return NM_ERR_OOM;
   }
-  if (cudaMalloc(&h->status, sizeof(uint32_t)) != cudaSuccess) {
+  if (cudaMalloc(&h->status, sizeof(uint32_t)) != cudaSuccess ||
+      cudaMalloc(&h->sched, sizeof(nm::Schedule)) != cudaSuccess) {
     cudaFree(h->blob);
+    if (h->status) cudaFree(h->status);
+    delete sc;
     delete h;
     return NM_ERR_OOM;
   }
-  if (cudaMemset(h->blob, 0, h->blob_size) != cudaSuccess ||
-      cudaMemset(h->status, 0, sizeof(uint32_t)) != cudaSuccess) {
+  const bool ok = cudaMemset(h->blob, 0, h->blob_size) == cudaSuccess &&
+                  cudaMemset(h->status, 0, sizeof(uint32_t)) == cudaSuccess &&
+                  cudaMemcpy(h->sched, sc, sizeof(nm::Schedule), cudaMemcpyHostToDevice) == cudaSuccess;
+  delete sc;
+  if (!ok) {
     cudaFree(h->blob);
     cudaFree(h->status);
+    cudaFree(h->sched);
     delete h;
     return NM_ERR_CUDA;
   }
+  p.sched = h->sched;
   p.blob = h->blob;
   p.status = h->status;
   *out = h;
@@ -342,7 +367,7 @@ nm_status nm_mlp_infer(nm_mlp* h, const void* in, int64_t n, void* out, nm_strea
   p.num_tiles = static_cast<int32_t>((n + nm::kTileM - 1) / nm::kTileM);
   p.wait_ns = h->wait_ns;
   p.test_stall = h->test_stall;
-  const uint32_t smem = nm::plan_fused_smem(p, h->variant, h->smem_optin);
+  const uint32_t smem = nm::plan_fused_smem(p, h->dims, h->variant, h->smem_optin);
   if (smem == 0) return NM_ERR_UNSUPPORTED;
   const int grid = p.num_tiles < h->num_sms ? p.num_tiles : h->num_sms;
   if (nm::launch_fused(p, h->variant, grid, smem, s) != cudaSuccess) return NM_ERR_CUDA;
@@ -386,6 +411,7 @@ void nm_mlp_destroy(nm_mlp* h) {
   cudaDeviceSynchronize();
   cudaFree(h->blob);
   cudaFree(h->status);
+  cudaFree(h->sched);
   if (h->mirror) cudaFree(h->mirror);
   delete h;
 }

@@ -3,18 +3,21 @@
 // One CTA per SM walks 128-sample tiles t = blockIdx.x, blockIdx.x + grid, ...
 // and runs every layer of the network on each tile without leaving the SM
 // ("Optimization Techniques: Squeezing the Silicon", "Kernel Fusion": one
-// write to memory, intermediates stay on chip). Roles, by warp:
-//   warp 0      producer: TMA loads of the [128 x d0] input tiles into a ring
-//               (and, in the row-major ablation, rebuilds every layer's B
-//               operand from the row-major weights for every tile);
-//   warp 1      one thread issues the tcgen05.mma chain of each layer,
-//               D[128 x N] (FP32, TMEM) = A[128 x K] (FP16, smem) * W^T;
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows, FP32 bias add,
-//               FP16 rounding, FP16 activation max(h, h*half(0.01)), and a
-//               16-byte store into the next layer's A tile (or into the
-//               output staging tile, which leaves by TMA store).
-// Two tiles are in flight (two TMEM accumulator slots, two activation tiles)
-// so one tile's epilogue overlaps the other tile's MMAs.
+// write to memory, intermediates stay on chip). Up to four tiles are in
+// flight per CTA (tile slots), each with its own TMEM accumulator and its own
+// activation tile in shared memory. Roles, by warp:
+//   warp 0       producer: TMA loads of the [128 x d0] input tiles into a ring
+//                (and, in the row-major ablation, rebuilds the B operand of
+//                every layer of every tile from the row-major weights);
+//   warp 1       one thread issues the tcgen05.mma chains. For each layer it
+//                issues that layer for every slot before waiting on any slot's
+//                epilogue, so one slot's MMAs overlap the others' epilogues:
+//                D[128 x N] (FP32, TMEM) = A[128 x K] (FP16, smem) * W^T;
+//   warps 2..17  epilogue, 16 warps split as slots x 4 TMEM lane quadrants x
+//                column groups: tcgen05.ld of the accumulator rows, FP32 bias
+//                add, FP16 rounding, FP16 activation max(h, h*half(0.01)),
+//                16-byte stores into the next layer's A tile (or into an
+//                output staging tile that the same warp sends out by TMA).
 //
 // The page "Profiling neural material inference" fixes the arithmetic
 // ("Experiment setup": the full layer chain per evaluation; "Bad versus good
@@ -22,11 +25,17 @@
 // here as variants: "Row-major versus InferencingOptimal weights" (B operand
 // rebuilt from row-major memory per tile) and the indexed-lane activation.
 //
+// All UMMA descriptors are precomputed on the host (the schedule) and copied
+// into shared memory once per CTA, so issuing one MMA is a 16-byte shared
+// load, two adds and the tcgen05.mma itself.
+//
 // Every wait is bounded by a wall-clock limit. A wait that gives up sets the
 // device status word and a CTA-wide abort flag; every role then stops, waits
 // (with a fixed limit) for its own copies and MMAs in flight, and the CTA
 // frees its tensor memory and exits.
 #include <cuda_fp16.h>
+
+#include <cstring>
 
 #include "nm_internal.h"
 #include "nm_ptx.cuh"
@@ -43,8 +52,12 @@ struct Ctx {
   uint8_t* gbase;                 // generic pointer to the byte at sbase
   volatile uint32_t* abort_flag;  // CTA-wide give-up flag
   uint32_t tmem;                  // TMEM base address
+  int32_t n_local;                // tiles this CTA processes
   __device__ __forceinline__ uint32_t bar(int i) const {
     return bars + static_cast<uint32_t>(i) * 8u;
+  }
+  __device__ __forceinline__ const Schedule* sched(const FusedParams& p) const {
+    return reinterpret_cast<const Schedule*>(gbase + p.sm_sched);
   }
 };
 
@@ -77,7 +90,14 @@ __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, uint32_t*
   }
 }
 
-// FP32 accumulator pair + FP32 bias pair -> FP16 pair (round to nearest even),
+// Warp-uniform bounded wait: every lane polls, the warp proceeds together.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const FusedParams& p,
+                                         const Ctx& c) {
+  const bool got = wait_phase(bar, parity, p.wait_ns, c.abort_flag, p.status);
+  return __all_sync(0xFFFFFFFFu, got);
+}
+
+// FP32 accumulator pairs + FP32 bias -> FP16 pairs (round to nearest even),
 // then the activation when `act` is set. Column 2j goes to the low half.
 template <int V>
 __device__ __forceinline__ void epilogue_chunk(const uint32_t* acc, const float* bias, int npairs,
@@ -86,7 +106,9 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t* acc, const float*
   for (int j = 0; j < 16; ++j) {
     if (j < npairs) {
       const float2 a = make_float2(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
-      const float2 b = *reinterpret_cast<const float2*>(bias + 2 * j);
+      // one 16-byte broadcast load serves two pairs
+      const float4 b4 = *reinterpret_cast<const float4*>(bias + 4 * (j >> 1));
+      const float2 b = (j & 1) ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
       const float2 v = __fadd2_rn(a, b);
       __half2 h = __float22half2_rn(v);
       if (V != kVarScalar) {
@@ -121,7 +143,7 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t* acc, const float*
 
 __device__ __forceinline__ void issue_input_tma(const FusedParams& p, uint32_t dst, uint32_t bar,
                                                 int32_t tile) {
-  const int K = p.dims[0];
+  const int K = p.d0;
   for (int k = 0; k < K;) {
     uint32_t off;
     int w, k0;
@@ -131,59 +153,75 @@ __device__ __forceinline__ void issue_input_tma(const FusedParams& p, uint32_t d
   }
 }
 
+__device__ __forceinline__ int32_t tile_of(int32_t i) {
+  return static_cast<int32_t>(blockIdx.x) + i * static_cast<int32_t>(gridDim.x);
+}
+
 // ------------------------------------------------------------------ producer
 template <int V>
 __device__ __forceinline__ void run_producer(const FusedParams& p, const Ctx& c, int lane) {
   const uint32_t R = p.n_in_stages;
+  const int32_t S = static_cast<int32_t>(p.n_slots);
   int32_t last_round[kMaxInStages];
 #pragma unroll
   for (int s = 0; s < kMaxInStages; ++s) last_round[s] = -1;
 
-  uint32_t i = 0, g = 0;
   bool ok = true;
-  for (int32_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++i) {
-    const uint32_t st = i % R, rnd = i / R;
-    if (lane == 0) {
-      ok = wait_phase(c.bar(kBarInEmpty + st), (rnd & 1u) ^ 1u, p.wait_ns, c.abort_flag, p.status);
-      if (ok) {
-        mbar_arrive_expect_tx(c.bar(kBarInFull + st), static_cast<uint32_t>(kTileM * 2 * p.dims[0]));
-        issue_input_tma(p, c.sbase + p.sm_in + st * p.in_stage_bytes, c.bar(kBarInFull + st), t);
-        last_round[st] = static_cast<int32_t>(rnd);
+  if (V == kVarRowMajor) ok = warp_wait(c.bar(kBarWLoad), 0, p, c);
+  uint32_t g = 0;
+  for (int32_t r = 0; r * S < c.n_local && ok; ++r) {
+    // Input tiles of this round, in tile order.
+    for (int32_t s = 0; s < S && ok; ++s) {
+      const int32_t i = r * S + s;
+      if (i >= c.n_local) break;
+      if (lane == 0) {
+        const uint32_t st = static_cast<uint32_t>(i) % R, rnd = static_cast<uint32_t>(i) / R;
+        ok = wait_phase(c.bar(kBarInEmpty + st), (rnd & 1u) ^ 1u, p.wait_ns, c.abort_flag, p.status);
+        if (ok) {
+          mbar_arrive_expect_tx(c.bar(kBarInFull + st), static_cast<uint32_t>(kTileM * 2 * p.d0));
+          issue_input_tma(p, c.sbase + p.sm_in + st * p.in_stage_bytes, c.bar(kBarInFull + st),
+                          tile_of(i));
+          last_round[st] = static_cast<int32_t>(rnd);
+        }
       }
     }
     if (V == kVarRowMajor) {
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      // Rebuild every layer's B operand for this tile from the row-major
-      // weights: 16-byte row-major loads, swizzled 16-byte smem stores.
-      for (int l = 0; l < p.L && ok; ++l, ++g) {
-        const uint32_t bs = g % p.n_b_stages, brnd = g / p.n_b_stages;
-        const bool got = wait_phase(c.bar(kBarBEmpty + bs), (brnd & 1u) ^ 1u, p.wait_ns,
-                                    c.abort_flag, p.status);
-        ok = __all_sync(0xFFFFFFFFu, got);
-        if (!ok) break;
-        const int K = p.dims[l], N = p.dims[l + 1], kc = K >> 3;
-        const uint16_t* Wl = p.mirror + p.rm_off[l];
-        const uint32_t stage = c.sbase + p.sm_b + bs * p.b_stage_bytes;
-        for (int idx = lane; idx < N * kc; idx += 32) {
-          const int n = idx / kc, col = (idx - n * kc) << 3;
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(Wl + n * K + col));
-          uint32_t off;
-          int w, k0;
-          locate(static_cast<uint32_t>(N), K, col, off, w, k0);
-          st_shared_v4(stage + off + swz(static_cast<uint32_t>(n * 2 * w + (col - k0) * 2), w),
-                       v.x, v.y, v.z, v.w);
+      // Rebuild every layer's B operand for every tile of this round from the
+      // row-major weights, in the order the MMA thread consumes them:
+      // 16-byte row-major loads, swizzled 16-byte smem stores.
+      const Schedule* sc = c.sched(p);
+      for (int l = 0; l < p.L && ok; ++l) {
+        const int K = sc->layer[l].K, N = sc->layer[l].N, kc = K >> 3;
+        const uint16_t* Wl = p.mirror + sc->layer[l].rm_off;
+        for (int32_t s = 0; s < S && ok; ++s) {
+          if (r * S + s >= c.n_local) break;
+          const uint32_t bs = g % p.n_b_stages, brnd = g / p.n_b_stages;
+          ok = warp_wait(c.bar(kBarBEmpty + bs), (brnd & 1u) ^ 1u, p, c);
+          if (!ok) break;
+          const uint32_t stage = c.sbase + p.sm_b + bs * p.b_stage_bytes;
+          for (int idx = lane; idx < N * kc; idx += 32) {
+            const int n = idx / kc, col = (idx - n * kc) << 3;
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(Wl + n * K + col));
+            uint32_t off;
+            int w, k0;
+            locate(static_cast<uint32_t>(N), K, col, off, w, k0);
+            st_shared_v4(stage + off + swz(static_cast<uint32_t>(n * 2 * w + (col - k0) * 2), w),
+                         v.x, v.y, v.z, v.w);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(c.bar(kBarBFull + bs));
+          ++g;
         }
-        fence_proxy_async_smem();
-        mbar_arrive(c.bar(kBarBFull + bs));
       }
     }
   }
   if (lane == 0) {
-    // Drain: every copy this warp issued (input tiles, and the one-time
-    // weight staging) must land before the CTA may exit.
+    // Drain: every copy this warp issued (input tiles, the one-time weight and
+    // schedule staging) must land before the CTA may exit.
     for (uint32_t s = 0; s < R; ++s)
       if (last_round[s] >= 0) wait_drain(c.bar(kBarInFull + s), last_round[s] & 1, p.status);
-    if (V != kVarRowMajor) wait_drain(c.bar(kBarWLoad), 0, p.status);
+    wait_drain(c.bar(kBarWLoad), 0, p.status);
   }
 }
 
@@ -191,59 +229,59 @@ __device__ __forceinline__ void run_producer(const FusedParams& p, const Ctx& c,
 template <int V>
 __device__ __forceinline__ void run_mma(const FusedParams& p, const Ctx& c) {
   const uint32_t R = p.n_in_stages;
+  const int32_t S = static_cast<int32_t>(p.n_slots);
   const int L = p.L;
   bool ok = true;
   if (p.test_stall) ok = wait_phase(c.bar(kBarNever), 0, p.wait_ns, c.abort_flag, p.status);
-  if (ok && V != kVarRowMajor)
-    ok = wait_phase(c.bar(kBarWLoad), 0, p.wait_ns, c.abort_flag, p.status);
-  uint32_t i = 0, g = 0;
-  for (int32_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++i) {
-    const uint32_t s = i & 1u, st = i % R, rnd = i / R;
-    const uint32_t d_tmem = c.tmem + s * p.nmax;
-    for (int l = 0; l < L; ++l) {
-      const int q = static_cast<int>((i >> 1) * L + l) - 1;
-      if (q >= 0 && !wait_phase(c.bar(kBarActReady + s), q & 1, p.wait_ns, c.abort_flag, p.status)) {
-        ok = false;
-        break;
-      }
-      if (l == 0 &&
-          !wait_phase(c.bar(kBarInFull + st), rnd & 1u, p.wait_ns, c.abort_flag, p.status)) {
-        ok = false;
-        break;
-      }
-      uint32_t b_base, bs = 0;
-      if (V == kVarRowMajor) {
-        bs = g % p.n_b_stages;
-        if (!wait_phase(c.bar(kBarBFull + bs), (g / p.n_b_stages) & 1u, p.wait_ns, c.abort_flag,
-                        p.status)) {
+  if (ok) ok = wait_phase(c.bar(kBarWLoad), 0, p.wait_ns, c.abort_flag, p.status);
+  const Schedule* sc = c.sched(p);
+  uint32_t g = 0;
+  for (int32_t r = 0; r * S < c.n_local && ok; ++r) {
+    for (int l = 0; l < L && ok; ++l) {
+      const uint32_t sb = sc->layer[l].slab_begin, se = sc->layer[l].slab_end;
+      const uint32_t idesc = sc->layer[l].idesc;
+      const uint32_t w_base = c.sbase + p.sm_w + sc->layer[l].w_off;
+      for (int32_t s = 0; s < S; ++s) {
+        const int32_t i = r * S + s;
+        if (i >= c.n_local) break;
+        const uint32_t st = static_cast<uint32_t>(i) % R;
+        const int32_t q = r * L + l - 1;  // completion of this slot's previous epilogue
+        if (q >= 0 && !wait_phase(c.bar(kBarActReady + s), static_cast<uint32_t>(q) & 1u, p.wait_ns,
+                                  c.abort_flag, p.status)) {
           ok = false;
           break;
         }
-        b_base = c.sbase + p.sm_b + bs * p.b_stage_bytes;
-      } else {
-        b_base = c.sbase + p.sm_w + p.w_off[l];
-      }
-      tc_fence_after_sync();
-      const uint32_t a_base = (l == 0) ? (c.sbase + p.sm_in + st * p.in_stage_bytes)
-                                       : (c.sbase + p.sm_act + s * p.act_slot_bytes);
-      const int K = p.dims[l], N = p.dims[l + 1];
-      const uint32_t idesc = idesc_f16_f32(kTileM, static_cast<uint32_t>(N));
-      for (int k = 0; k < K; k += 16) {
-        uint32_t aoff, boff;
-        int w, k0;
-        locate(kTileM, K, k, aoff, w, k0);
-        locate(static_cast<uint32_t>(N), K, k, boff, w, k0);
-        const uint32_t kb = static_cast<uint32_t>(k - k0) * 2u;
-        const uint32_t sbo = 16u * static_cast<uint32_t>(w);
-        const uint64_t adesc = smem_desc(a_base + aoff + kb, sbo, swizzle_code(w));
-        const uint64_t bdesc = smem_desc(b_base + boff + kb, sbo, swizzle_code(w));
-        umma_f16_ss(d_tmem, adesc, bdesc, idesc, k > 0 ? 1u : 0u);
-      }
-      umma_commit(c.bar(kBarAccFull + s));
-      if (l == 0) umma_commit(c.bar(kBarInEmpty + st));
-      if (V == kVarRowMajor) {
-        umma_commit(c.bar(kBarBEmpty + bs));
-        ++g;
+        if (l == 0 && !wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(i) / R) & 1u,
+                                  p.wait_ns, c.abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        uint32_t b_base = w_base, bs = 0;
+        if (V == kVarRowMajor) {
+          bs = g % p.n_b_stages;
+          if (!wait_phase(c.bar(kBarBFull + bs), (g / p.n_b_stages) & 1u, p.wait_ns, c.abort_flag,
+                          p.status)) {
+            ok = false;
+            break;
+          }
+          b_base = c.sbase + p.sm_b + bs * p.b_stage_bytes;
+        }
+        tc_fence_after_sync();
+        const uint32_t a_base =
+            (l == 0) ? (c.sbase + p.sm_in + st * p.in_stage_bytes)
+                     : (c.sbase + p.sm_act + static_cast<uint32_t>(s) * p.act_slot_bytes);
+        const uint64_t a_add = a_base >> 4, b_add = b_base >> 4;
+        const uint32_t d_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
+        for (uint32_t j = sb; j < se; ++j) {
+          const SlabDesc sd = sc->slab[j];
+          umma_f16_ss(d_tmem, sd.a + a_add, sd.b + b_add, idesc, j > sb ? 1u : 0u);
+        }
+        umma_commit(c.bar(kBarAccFull + s));
+        if (l == 0) umma_commit(c.bar(kBarInEmpty + st));
+        if (V == kVarRowMajor) {
+          umma_commit(c.bar(kBarBEmpty + bs));
+          ++g;
+        }
       }
     }
   }
@@ -253,42 +291,67 @@ __device__ __forceinline__ void run_mma(const FusedParams& p, const Ctx& c) {
 }
 
 // ------------------------------------------------------------------ epilogue
+// Output staging of one tile: a region per 32-column chunk of the output
+// (128 rows x 64 bytes, 64-byte swizzle; a trailing 16-column chunk gets
+// 128 x 32 bytes, 32-byte swizzle), each 1024-aligned. A warp stores the rows
+// of its lane quadrant of its own chunks with its own TMA stores, so no warp
+// ever waits for another.
+__device__ __forceinline__ uint32_t out_chunk_off(int c0) {
+  return static_cast<uint32_t>(c0 >> 5) * (kTileM * 64u);
+}
+
+// Epilogue warp e serves tile slot e / (4G), column group (e % 4G) / 4 and
+// TMEM lane quadrant (warp index % 4), where G = 16 / (4 * slots) column
+// groups share the columns of a layer in 32-column chunks g, g + G, ...
 template <int V>
 __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c, int warp,
                                              int lane) {
+  const int32_t S = static_cast<int32_t>(p.n_slots);
+  const int G = kEpiWarps / (4 * S);
+  const int e = warp - 2;
+  const int32_t s = e / (4 * G);
+  const int g = (e % (4 * G)) / 4;
   const int quad = warp & 3;  // TMEM lane quadrant this warp may access
   const uint32_t row = static_cast<uint32_t>(quad * 32 + lane);
   const uint32_t lane_bits = static_cast<uint32_t>(quad * 32) << 16;
   const __half2 slope2 = __float2half2_rn(0.01f);  // half(0.01)
   const float* sbias = reinterpret_cast<const float*>(c.gbase + p.sm_bias);
   const int L = p.L;
-  uint32_t i = 0;
-  for (int32_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++i) {
-    const uint32_t s = i & 1u;
+  const int n_out = p.dL;
+  const bool storer = (lane == 0) && (32 * g < n_out);
+  if (!warp_wait(c.bar(kBarWLoad), 0, p, c)) return;
+  const Schedule* sc = c.sched(p);
+  const uint32_t act_dst = c.sbase + p.sm_act + static_cast<uint32_t>(s) * p.act_slot_bytes;
+  const uint32_t tbase = c.tmem + lane_bits + static_cast<uint32_t>(s) * p.slot_cols;
+  for (int32_t r = 0; r * S + s < c.n_local; ++r) {
+    const int32_t t = tile_of(r * S + s);
     bool ok = true;
     for (int l = 0; l < L; ++l) {
-      const uint32_t q = (i >> 1) * static_cast<uint32_t>(L) + static_cast<uint32_t>(l);
-      // All lanes poll; the warp proceeds only together (the TMEM loads below
-      // are warp-collective).
-      const bool got = wait_phase(c.bar(kBarAccFull + s), q & 1u, p.wait_ns, c.abort_flag, p.status);
-      if (!__all_sync(0xFFFFFFFFu, got)) {
+      const uint32_t q = static_cast<uint32_t>(r * L + l);
+      if (!warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      const int N = p.dims[l + 1];
+      const int N = sc->layer[l].N;
       const bool last = (l == L - 1);
-      const float* bias = sbias + p.bias_f_off[l];
-      const uint32_t dst = last ? (c.sbase + p.sm_out + s * p.out_slot_bytes)
-                                : (c.sbase + p.sm_act + s * p.act_slot_bytes);
+      const float* bias = sbias + sc->layer[l].bias_f_off;
+      const uint32_t out_dst =
+          c.sbase + p.sm_out +
+          (static_cast<uint32_t>(s) * p.n_out_bufs + static_cast<uint32_t>(r) % p.n_out_bufs) *
+              p.out_slot_bytes;
       if (last) {
-        // The staging tile of slot s was last handed to a TMA store kSlots
-        // tiles ago; make sure that store has finished reading it.
-        if (lane == 0) bulk_wait_group_read<kSlots - 1>();
+        // This staging buffer went to this warp's TMA stores n_out_bufs tiles
+        // of this slot ago; they must have finished reading it.
+        if (storer) {
+          if (p.n_out_bufs > 1)
+            bulk_wait_group_read<1>();
+          else
+            bulk_wait_group_read<0>();
+        }
         __syncwarp();
       }
-      const uint32_t tbase = c.tmem + lane_bits + s * p.nmax;
-      for (int c0 = 0; c0 < N; c0 += 32) {
+      for (int c0 = 32 * g; c0 < N; c0 += 32 * G) {
         uint32_t acc[32];
         uint32_t h[16];
         const int cols = (N - c0 >= 32) ? 32 : 16;
@@ -299,17 +362,25 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
         }
         tmem_wait_ld();
         epilogue_chunk<V>(acc, bias + c0, cols >> 1, !last, slope2, h);
+        if (last) {
+          const uint32_t base = out_dst + out_chunk_off(c0);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          if (cc * 8 < cols) {
-            const int col = c0 + cc * 8;
-            uint32_t off;
-            int w, k0;
-            locate(kTileM, N, col, off, w, k0);
-            const uint32_t lin = row * 2u * static_cast<uint32_t>(w) + static_cast<uint32_t>(col - k0) * 2u;
-            st_shared_v4(dst + off + swz(lin, w), h[4 * cc], h[4 * cc + 1], h[4 * cc + 2],
-                         h[4 * cc + 3]);
-          }
+          for (int cc = 0; cc < 4; ++cc)
+            if (cc * 8 < cols)
+              st_shared_v4_nc(base + swz(row * 2u * static_cast<uint32_t>(cols) + cc * 16u, cols),
+                              h[4 * cc], h[4 * cc + 1], h[4 * cc + 2], h[4 * cc + 3]);
+        } else {
+          uint32_t off;
+          int w, k0;
+          locate(kTileM, N, c0, off, w, k0);  // a 32-column chunk never straddles segments
+          const uint32_t base = act_dst + off;
+          const uint32_t lin0 =
+              row * 2u * static_cast<uint32_t>(w) + static_cast<uint32_t>(c0 - k0) * 2u;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            if (cc * 8 < cols)
+              st_shared_v4_nc(base + swz(lin0 + cc * 16u, w), h[4 * cc], h[4 * cc + 1],
+                              h[4 * cc + 2], h[4 * cc + 3]);
         }
       }
       tc_fence_before_sync();
@@ -317,17 +388,14 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
       mbar_arrive(c.bar(kBarActReady + s));
       if (last) {
         __syncwarp();
-        if (lane == 0) {
+        if (storer) {
           const int64_t row0 = static_cast<int64_t>(t) * kTileM + quad * 32;
           if (row0 < p.n) {
-            for (int k = 0; k < N;) {
-              uint32_t off;
-              int w, k0;
-              locate(kTileM, N, k, off, w, k0);
-              tma_store_2d(&p.tm_out[swizzle_kind(w)],
-                           dst + off + static_cast<uint32_t>(quad * 32) * 2u * static_cast<uint32_t>(w),
-                           k0, static_cast<int32_t>(row0));
-              k = k0 + w;
+            for (int c0 = 32 * g; c0 < N; c0 += 32 * G) {
+              const int cols = (N - c0 >= 32) ? 32 : 16;
+              tma_store_2d(&p.tm_out[swizzle_kind(cols)],
+                           out_dst + out_chunk_off(c0) + static_cast<uint32_t>(quad * 32 * 2 * cols),
+                           c0, static_cast<int32_t>(row0));
             }
           }
           bulk_commit_group();
@@ -336,7 +404,7 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
     }
     if (!ok) break;
   }
-  if (lane == 0) bulk_wait_group_all();
+  if (storer) bulk_wait_group_all();
 }
 
 template <int V>
@@ -349,17 +417,23 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   c.gbase = smem_raw + (c.sbase - raw);
   c.bars = c.sbase + p.sm_bar;
   c.abort_flag = reinterpret_cast<volatile uint32_t*>(c.gbase + p.sm_bar + kAbortOff);
+  c.n_local = (static_cast<int32_t>(blockIdx.x) < p.num_tiles)
+                  ? (p.num_tiles - static_cast<int32_t>(blockIdx.x) +
+                     static_cast<int32_t>(gridDim.x) - 1) /
+                        static_cast<int32_t>(gridDim.x)
+                  : 0;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(c.gbase + p.sm_bar + kTmemSlotOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    const uint32_t epi_per_slot = 32u * kEpiWarps / p.n_slots;
     for (int s = 0; s < kMaxInStages; ++s) {
       mbar_init(c.bar(kBarInFull + s), 1);
       mbar_init(c.bar(kBarInEmpty + s), 1);
     }
-    for (int s = 0; s < kSlots; ++s) {
+    for (int s = 0; s < kMaxSlots; ++s) {
       mbar_init(c.bar(kBarAccFull + s), 1);
-      mbar_init(c.bar(kBarActReady + s), 128);
+      mbar_init(c.bar(kBarActReady + s), epi_per_slot);
     }
     for (int s = 0; s < kMaxBStages; ++s) {
       mbar_init(c.bar(kBarBFull + s), 32);
@@ -387,11 +461,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   c.tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (V != kVarRowMajor && lane == 0) {
-      // Stage the packed weight images once for the whole persistent loop.
-      mbar_arrive_expect_tx(c.bar(kBarWLoad), p.bias_off);
-      for (uint32_t off = 0; off < p.bias_off; off += 32768u) {
-        const uint32_t bytes = (p.bias_off - off) < 32768u ? (p.bias_off - off) : 32768u;
+    if (lane == 0) {
+      // Stage the schedule (and the packed weight images) once for the whole
+      // persistent loop.
+      const uint32_t wbytes = (V == kVarRowMajor) ? 0u : p.bias_off;
+      mbar_arrive_expect_tx(c.bar(kBarWLoad), p.sched_bytes + wbytes);
+      bulk_load(c.sbase + p.sm_sched, p.sched, p.sched_bytes, c.bar(kBarWLoad));
+      for (uint32_t off = 0; off < wbytes; off += 32768u) {
+        const uint32_t bytes = (wbytes - off) < 32768u ? (wbytes - off) : 32768u;
         bulk_load(c.sbase + p.sm_w + off, p.blob + off, bytes, c.bar(kBarWLoad));
       }
     }
@@ -414,64 +491,111 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 }  // namespace
 
 // ------------------------------------------------------------------ host side
-uint32_t plan_fused_smem(FusedParams& p, int variant, uint32_t smem_optin) {
+uint32_t build_schedule(const int32_t* dims, int L, const uint32_t* w_off, const uint32_t* rm_off,
+                        Schedule& sc) {
+  std::memset(&sc, 0, sizeof(sc));
+  uint32_t slab = 0, nb = 0;
+  for (int l = 0; l < L; ++l) {
+    const int K = dims[l], N = dims[l + 1];
+    LayerInfo& li = sc.layer[l];
+    li.K = K;
+    li.N = N;
+    li.slab_begin = slab;
+    li.idesc = idesc_f16_f32(kTileM, static_cast<uint32_t>(N));
+    li.bias_f_off = nb;
+    li.rm_off = rm_off[l];
+    li.w_off = w_off[l];
+    for (int k = 0; k < K; k += 16) {
+      uint32_t aoff, boff;
+      int w, k0;
+      locate(kTileM, K, k, aoff, w, k0);
+      locate(static_cast<uint32_t>(N), K, k, boff, w, k0);
+      const uint32_t kb = static_cast<uint32_t>(k - k0) * 2u;
+      const uint32_t sbo = 16u * static_cast<uint32_t>(w);
+      sc.slab[slab].a = smem_desc(aoff + kb, sbo, swizzle_code(w));
+      sc.slab[slab].b = smem_desc(boff + kb, sbo, swizzle_code(w));
+      ++slab;
+    }
+    li.slab_end = slab;
+    nb += static_cast<uint32_t>(N);
+  }
+  return static_cast<uint32_t>(sizeof(LayerInfo) * kMaxLayers + sizeof(SlabDesc) * slab);
+}
+
+uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint32_t smem_optin) {
   const int L = p.L;
   uint32_t nmax = 0, act_w = 16, bstage = 0, nb = 0;
   for (int l = 0; l < L; ++l) {
-    const uint32_t N = static_cast<uint32_t>(p.dims[l + 1]);
+    const uint32_t N = static_cast<uint32_t>(dims[l + 1]);
     nmax = N > nmax ? N : nmax;
     if (l < L - 1 && N > act_w) act_w = N;
-    const uint32_t ib = image_bytes(N, p.dims[l]);
+    const uint32_t ib = image_bytes(N, dims[l]);
     bstage = ib > bstage ? ib : bstage;
-    p.bias_f_off[l] = nb;
     nb += N;
   }
   p.n_bias = nb;
-  // TMEM columns per tile slot: the widest layer, rounded up to a power of two.
-  uint32_t slot = 32;
+  p.d0 = dims[0];
+  p.dL = dims[L];
+  uint32_t slot = 32;  // TMEM columns per slot: the widest layer, as a power of two
   while (slot < nmax) slot <<= 1;
-  p.nmax = slot;
-  uint32_t cols = 32;
-  while (cols < kSlots * slot) cols <<= 1;
-  if (cols > 512) return 0;
-  p.tmem_cols = cols;
+  p.slot_cols = slot;
 
-  p.in_stage_bytes = image_bytes(kTileM, p.dims[0]);
   p.act_slot_bytes = align1024(image_bytes(kTileM, static_cast<int>(act_w)));
-  p.out_slot_bytes = align1024(image_bytes(kTileM, p.dims[L]));
+  // output staging: 8 KB per 32-column chunk, 4 KB for a trailing 16-column one
+  p.out_slot_bytes = static_cast<uint32_t>(p.dL >> 5) * (kTileM * 64u) +
+                     ((p.dL & 31) ? kTileM * 32u : 0u);
   p.b_stage_bytes = (variant == kVarRowMajor) ? align1024(bstage) : 0u;
   p.n_b_stages = (variant == kVarRowMajor) ? kMaxBStages : 0u;
+  const uint32_t stage = align1024(image_bytes(kTileM, p.d0));
 
-  uint32_t off = 0;
-  p.sm_w = 0;
-  off += (variant == kVarRowMajor) ? 0u : align1024(p.bias_off);
-  p.sm_bias = off;
-  off += align1024(nb * 4u);
-  p.sm_act = off;
-  off += kSlots * p.act_slot_bytes;
-  p.sm_out = off;
-  off += kSlots * p.out_slot_bytes;
-  p.sm_b = off;
-  off += p.n_b_stages * p.b_stage_bytes;
-  p.sm_bar = off;
-  off += 1024u;  // barrier block (256 B used), keeps the input ring 1024-aligned
-  p.sm_in = off;
-  const uint32_t fixed = off + 1024u;  // + alignment slack of the dynamic smem base
-  int stages = kMaxInStages;
-  while (stages >= 2 && fixed + static_cast<uint32_t>(stages) * align1024(p.in_stage_bytes) > smem_optin)
-    --stages;
-  if (stages < 2) return 0;
-  p.in_stage_bytes = align1024(p.in_stage_bytes);
-  p.n_in_stages = static_cast<uint32_t>(stages);
-  return fixed + static_cast<uint32_t>(stages) * p.in_stage_bytes;
+  // Most tile slots first (4, 2, 1) as TMEM allows, then two output buffers
+  // before one, then the deepest input ring (4 down to 2) that fits.
+  for (uint32_t slots = kMaxSlots; slots >= 1; slots >>= 1) {
+    if (slots * slot > 512u) continue;
+    for (uint32_t obufs = kOutBufs; obufs >= 1; --obufs) {
+      uint32_t off = 0;
+      p.sm_w = 0;
+      off += (variant == kVarRowMajor) ? 0u : align1024(p.bias_off);
+      p.sm_sched = off;
+      off += align1024(p.sched_bytes);
+      p.sm_bias = off;
+      off += align1024(nb * 4u);
+      p.sm_act = off;
+      off += slots * p.act_slot_bytes;
+      p.sm_out = off;
+      off += slots * obufs * p.out_slot_bytes;
+      p.sm_b = off;
+      off += p.n_b_stages * p.b_stage_bytes;
+      p.sm_bar = off;
+      off += 1024u;  // barrier block, keeps the input ring 1024-aligned
+      p.sm_in = off;
+      const uint32_t fixed = off + 1024u;  // + alignment slack of the dynamic smem base
+      for (uint32_t stages = kMaxInStages; stages >= 2; --stages) {
+        if (fixed + stages * stage <= smem_optin) {
+          uint32_t cols = 32;
+          while (cols < slots * slot) cols <<= 1;
+          p.tmem_cols = cols;
+          p.n_slots = slots;
+          p.in_stage_bytes = stage;
+          p.n_in_stages = stages;
+          p.n_out_bufs = obufs;
+          return fixed + stages * stage;
+        }
+      }
+    }
+  }
+  return 0;
 }
 
 template <int V>
 static cudaError_t launch_variant(const FusedParams& p, int grid, uint32_t smem, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fused_mlp_kernel<V>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fused_mlp_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
     if (e != cudaSuccess) return e;
     configured = true;
   }

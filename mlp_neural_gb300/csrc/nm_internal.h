@@ -1,5 +1,6 @@
 // nm_internal.h -- declarations shared by the translation units of libnmmlp
-// (kernel parameter blocks and launchers). Not part of the public ABI.
+// (kernel parameter blocks, the per-network schedule table, launchers).
+// Not part of the public ABI.
 #pragma once
 
 #include <cstdint>
@@ -10,10 +11,14 @@
 
 namespace nm {
 
-constexpr int kSlots = 2;          // 128-sample tiles in flight per CTA
+constexpr int kMaxSlots = 4;       // 128-sample tiles in flight per CTA (upper bound)
 constexpr int kMaxInStages = 4;    // input TMA ring depth (upper bound)
 constexpr int kMaxBStages = 4;     // B-operand ring depth of the row-major ablation
-constexpr int kFusedThreads = 192; // warp 0 producer, warp 1 MMA, warps 2-5 epilogue
+constexpr int kEpiWarps = 16;      // epilogue warps: slots x 4 lane quadrants x column groups
+// warp 0 producer, warp 1 MMA issuer, then the epilogue warps
+constexpr int kFusedThreads = 64 + 32 * kEpiWarps;
+constexpr int kOutBufs = 2;        // output staging buffers per slot (TMA-store double buffer)
+constexpr int kMaxSlabs = kMaxLayers * (kMaxDim / 16);
 constexpr uint32_t kStatusTimeout = 1u;
 
 enum Variant : int { kVarFused = 0, kVarRowMajor = 1, kVarScalar = 2 };
@@ -23,46 +28,77 @@ enum BarIndex : int {
   kBarInFull = 0,
   kBarInEmpty = kBarInFull + kMaxInStages,
   kBarAccFull = kBarInEmpty + kMaxInStages,
-  kBarActReady = kBarAccFull + kSlots,
-  kBarBFull = kBarActReady + kSlots,
+  kBarActReady = kBarAccFull + kMaxSlots,
+  kBarBFull = kBarActReady + kMaxSlots,
   kBarBEmpty = kBarBFull + kMaxBStages,
   kBarWLoad = kBarBEmpty + kMaxBStages,
   kBarDrain = kBarWLoad + 1,
   kBarNever = kBarDrain + 1,  // never signalled (failure-path test hook)
   kBarCount = kBarNever + 1
 };
-constexpr uint32_t kBarBlockBytes = 256;  // kBarCount * 8 barriers, then TMEM address and abort flag
-constexpr uint32_t kTmemSlotOff = 192;
-constexpr uint32_t kAbortOff = 196;
+constexpr uint32_t kTmemSlotOff = 256;  // barriers first, then the TMEM address and abort flag
+constexpr uint32_t kAbortOff = 260;
 static_assert(kBarCount * 8 <= kTmemSlotOff, "barrier block overflow");
+
+// Per-layer schedule entry (host-built, copied to smem once per CTA).
+struct LayerInfo {
+  int32_t K, N;
+  uint32_t slab_begin, slab_end;  // range of this layer's k-slabs in the descriptor table
+  uint32_t idesc;                 // tcgen05 instruction descriptor (M = 128, N)
+  uint32_t bias_f_off;            // float offset of b_l in the smem bias array
+  uint32_t rm_off;                // element offset of W_l in the row-major mirror
+  uint32_t w_off;                 // byte offset of W_l's image in the blob / smem weight region
+};
+
+// UMMA shared-memory descriptors of one 16-wide k-slab, with start addresses
+// relative to a base that the kernel adds at issue time: A relative to the
+// layer's A tile, B relative to the layer's B image (resident weights or the
+// row-major ablation's B stage).
+struct SlabDesc {
+  uint64_t a;
+  uint64_t b;
+};
+
+struct Schedule {
+  LayerInfo layer[kMaxLayers];
+  SlabDesc slab[kMaxSlabs];
+};
+static_assert(sizeof(LayerInfo) == 32, "layer table entry size");
+static_assert(sizeof(Schedule) % 16 == 0, "schedule must copy in 16-byte units");
+
+// Fills the schedule for a network and returns the number of bytes of it the
+// kernel copies to shared memory (layer table + the slabs in use).
+uint32_t build_schedule(const int32_t* dims, int L, const uint32_t* w_off, const uint32_t* rm_off,
+                        Schedule& s);
 
 struct FusedParams {  // 128-byte aligned through its CUtensorMap members
   CUtensorMap tm_in[3];   // input [n][d0] maps, by swizzle kind (box 128 rows)
   CUtensorMap tm_out[3];  // output [n][dL] maps, by swizzle kind (box 32 rows)
   const uint8_t* blob;    // packed weight images + FP16 biases
+  const uint8_t* sched;   // Schedule (device copy)
   const uint16_t* mirror; // row-major weights (row-major ablation only)
   uint32_t* status;       // device status word
   int64_t n;
   int32_t num_tiles;
   int32_t L;
-  int32_t dims[kMaxLayers + 1];
-  uint32_t w_off[kMaxLayers];       // byte offset of layer l's image in blob / smem weight region
-  uint32_t rm_off[kMaxLayers];      // element offset of W_l in the mirror
-  uint32_t bias_f_off[kMaxLayers];  // float offset of b_l in the smem bias array
-  uint32_t bias_off;                // byte offset of the bias block in the blob
-  uint32_t n_bias;                  // sum of d_1..d_L
+  int32_t d0, dL;
+  uint32_t bias_off;      // byte offset of the bias block in the blob (= weight image bytes)
+  uint32_t n_bias;        // sum of d_1..d_L
+  uint32_t sched_bytes;   // bytes of the schedule to copy
   // shared-memory plan (byte offsets from the 1024-aligned base)
-  uint32_t sm_w, sm_bias, sm_in, sm_act, sm_out, sm_b, sm_bar;
+  uint32_t sm_w, sm_sched, sm_bias, sm_in, sm_act, sm_out, sm_b, sm_bar;
   uint32_t in_stage_bytes, act_slot_bytes, out_slot_bytes, b_stage_bytes;
-  uint32_t n_in_stages, n_b_stages;
-  uint32_t tmem_cols;  // allocated TMEM columns (power of two)
-  uint32_t nmax;       // TMEM columns per tile slot (max layer width)
-  uint64_t wait_ns;    // limit of every pipeline wait
-  uint32_t test_stall; // non-zero: the MMA thread first waits on kBarNever
+  uint32_t n_in_stages, n_b_stages, n_out_bufs;
+  uint32_t n_slots;     // tiles in flight (1, 2 or 4); kEpiWarps / (4 * n_slots) column groups
+  uint32_t tmem_cols;   // allocated TMEM columns (power of two)
+  uint32_t slot_cols;   // TMEM columns per tile slot
+  uint64_t wait_ns;     // limit of every pipeline wait
+  uint32_t test_stall;  // non-zero: the MMA thread first waits on kBarNever
 };
 
-// Returns the dynamic smem bytes the plan needs, or 0 if it does not fit.
-uint32_t plan_fused_smem(FusedParams& p, int variant, uint32_t smem_optin);
+// Chooses slots, stages and buffers for the network (dims[0..L]) and fills
+// the smem plan of `p`. Returns the dynamic smem bytes, or 0 if no plan fits.
+uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint32_t smem_optin);
 
 cudaError_t launch_fused(const FusedParams& p, int variant, int grid, uint32_t smem,
                          cudaStream_t stream);

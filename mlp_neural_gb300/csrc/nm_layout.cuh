@@ -86,4 +86,31 @@ __host__ __device__ __forceinline__ uint32_t image_bytes(uint32_t rows, int K) {
   return off;
 }
 
+// Shared-memory matrix descriptor (tcgen05 format): start address >> 4 in bits
+// [0,14), leading byte offset >> 4 in [16,30) (unused by the swizzled K-major
+// layouts used here; set to 1), stride byte offset >> 4 in [32,46) (distance
+// between consecutive 8-row core-matrix groups, 16w bytes for a w-wide
+// segment), the fixed version field 1 at bit 46, base offset 0, and the
+// swizzle mode in [61,64): 2 = 128-byte, 4 = 64-byte, 6 = 32-byte.
+// A descriptor built from an offset relative to some 1024-aligned base becomes
+// absolute by adding base >> 4 (the start field never carries past bit 13 for
+// addresses inside the 228 KB shared window).
+__host__ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo_bytes,
+                                                       uint32_t swizzle_code) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1u) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(swizzle_code & 7u) << 61;
+  return d;
+}
+
+// Instruction descriptor for kind::f16 with FP16 A and B, FP32 accumulator,
+// both operands K-major, dense: D format in bits [4,6) = 1 (F32), A/B formats
+// [7,10)/[10,13) = 0 (F16), N >> 3 in [17,23), M >> 4 in [24,29).
+__host__ __device__ __forceinline__ uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
 }  // namespace nm

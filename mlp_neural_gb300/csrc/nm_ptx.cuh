@@ -9,6 +9,8 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include "nm_layout.cuh"
+
 namespace nm {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -49,6 +51,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+// Named barrier among `count` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------- fences
@@ -190,29 +197,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-// ---------------------------------------------------------------- descriptors
-// Shared-memory matrix descriptor (tcgen05 format): start address >> 4 in bits
-// [0,14), leading byte offset >> 4 in [16,30) (unused by the swizzled K-major
-// layouts used here; set to 1), stride byte offset >> 4 in [32,46) (distance
-// between consecutive 8-row core-matrix groups), the fixed version field 1 at
-// bit 46, base offset 0, and the swizzle mode in [61,64):
-// 2 = 128-byte, 4 = 64-byte, 6 = 32-byte.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo_bytes,
-                                              uint32_t swizzle_code) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(1u) << 16;
-  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1u) << 46;
-  d |= static_cast<uint64_t>(swizzle_code & 7u) << 61;
-  return d;
-}
-
-// Instruction descriptor for kind::f16 with FP16 A and B, FP32 accumulator,
-// both operands K-major, dense: D format in bits [4,6) = 1 (F32), A/B formats
-// [7,10)/[10,13) = 0 (F16), N >> 3 in [17,23), M >> 4 in [24,29).
-__host__ __device__ __forceinline__ uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
-  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+// The same store without a compiler memory clobber: ordering against the
+// fences and barrier arrivals that follow it comes from those being volatile
+// asm statements too; ordinary loads may be scheduled across it.
+__device__ __forceinline__ void st_shared_v4_nc(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                                uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d));
 }
 
 }  // namespace nm
