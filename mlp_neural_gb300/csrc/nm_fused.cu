@@ -4,20 +4,24 @@
 // and runs every layer of the network on each tile without leaving the SM
 // ("Optimization Techniques: Squeezing the Silicon", "Kernel Fusion": one
 // write to memory, intermediates stay on chip). Up to four tiles are in
-// flight per CTA (tile slots), each with its own TMEM accumulator and its own
-// activation tile in shared memory. Roles, by warp:
+// flight per CTA (tile slots). A slot owns a TMEM region holding its FP32
+// accumulator and, beside it, the FP16 activations that feed the next layer
+// as the tensor core's A operand; only the input tile (layer 1's A), the
+// weights and the output staging live in shared memory. Roles, by warp:
 //   warp 0       producer: TMA loads of the [128 x d0] input tiles into a ring
 //                (and, in the row-major ablation, rebuilds the B operand of
 //                every layer of every tile from the row-major weights);
 //   warp 1       one thread issues the tcgen05.mma chains. For each layer it
 //                issues that layer for every slot before waiting on any slot's
 //                epilogue, so one slot's MMAs overlap the others' epilogues:
-//                D[128 x N] (FP32, TMEM) = A[128 x K] (FP16, smem) * W^T;
+//                D[128 x N] (FP32, TMEM) = A[128 x K] (FP16; smem for layer 1,
+//                TMEM after) * W^T (smem);
 //   warps 2..17  epilogue, 16 warps split as slots x 4 TMEM lane quadrants x
 //                column groups: tcgen05.ld of the accumulator rows, FP32 bias
 //                add, FP16 rounding, FP16 activation max(h, h*half(0.01)),
-//                16-byte stores into the next layer's A tile (or into an
-//                output staging tile that the same warp sends out by TMA).
+//                tcgen05.st of the FP16 pairs into the slot's A region (or,
+//                after the last layer, 16-byte stores into an output staging
+//                tile that the same warp sends out by TMA).
 //
 // The page "Profiling neural material inference" fixes the arithmetic
 // ("Experiment setup": the full layer chain per evaluation; "Bad versus good
@@ -59,13 +63,41 @@ struct Ctx {
   __device__ __forceinline__ const Schedule* sched(const FusedParams& p) const {
     return reinterpret_cast<const Schedule*>(gbase + p.sm_sched);
   }
+  // Shared-window address of field `off` of layer l's LayerInfo.
+  __device__ __forceinline__ uint32_t layer_addr(const FusedParams& p, int l) const {
+    return sbase + p.sm_sched + static_cast<uint32_t>(l) * static_cast<uint32_t>(sizeof(LayerInfo));
+  }
+  __device__ __forceinline__ uint32_t slab_addr(const FusedParams& p, uint32_t j) const {
+    return sbase + p.sm_sched + static_cast<uint32_t>(sizeof(LayerInfo) * kMaxLayers) +
+           j * static_cast<uint32_t>(sizeof(SlabDesc));
+  }
 };
+
+// LayerInfo as loaded from shared memory (two 16-byte loads).
+struct LayerRegs {
+  int32_t K, N;
+  uint32_t slab_begin, slab_end, idesc, bias_f_off, rm_off, w_off;
+};
+
+__device__ __forceinline__ LayerRegs load_layer(const FusedParams& p, const Ctx& c, int l) {
+  const uint32_t a = c.layer_addr(p, l);
+  const uint4 x = ld_shared_u32x4(a), y = ld_shared_u32x4(a + 16);
+  LayerRegs r;
+  r.K = static_cast<int32_t>(x.x);
+  r.N = static_cast<int32_t>(x.y);
+  r.slab_begin = x.z;
+  r.slab_end = x.w;
+  r.idesc = y.x;
+  r.bias_f_off = y.y;
+  r.rm_off = y.z;
+  r.w_off = y.w;
+  return r;
+}
 
 // Bounded wait on an mbarrier phase. Gives up (and raises the abort flag and
 // the status word) when `limit_ns` passes or another role has given up.
-__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                        volatile uint32_t* abort_flag, uint32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                             volatile uint32_t* abort_flag, uint32_t* status) {
   const uint64_t t0 = globaltimer_ns();
   uint32_t spins = 0;
   while (true) {
@@ -77,6 +109,12 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, uint64_t 
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                           volatile uint32_t* abort_flag, uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;  // fast path, inline
+  return wait_phase_slow(bar, parity, limit_ns, abort_flag, status);
 }
 
 // Wait used while draining: ignores the abort flag, fixed limit.
@@ -100,14 +138,14 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const F
 // FP32 accumulator pairs + FP32 bias -> FP16 pairs (round to nearest even),
 // then the activation when `act` is set. Column 2j goes to the low half.
 template <int V>
-__device__ __forceinline__ void epilogue_chunk(const uint32_t* acc, const float* bias, int npairs,
+__device__ __forceinline__ void epilogue_chunk(const uint32_t* acc, uint32_t bias_addr, int npairs,
                                                bool act, __half2 slope2, uint32_t* out) {
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     if (j < npairs) {
       const float2 a = make_float2(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
       // one 16-byte broadcast load serves two pairs
-      const float4 b4 = *reinterpret_cast<const float4*>(bias + 4 * (j >> 1));
+      const float4 b4 = ld_shared_f32x4(bias_addr + 16u * static_cast<uint32_t>(j >> 1));
       const float2 b = (j & 1) ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
       const float2 v = __fadd2_rn(a, b);
       __half2 h = __float22half2_rn(v);
@@ -157,137 +195,123 @@ __device__ __forceinline__ int32_t tile_of(int32_t i) {
   return static_cast<int32_t>(blockIdx.x) + i * static_cast<int32_t>(gridDim.x);
 }
 
-// ------------------------------------------------------------------ producer
+// ------------------------------------------------------------------ slot control
+// Control warp of tile slot s (warp index s). Its lane 0 keeps the slot's own
+// input ring (p.n_in_stages stages, rounds r, r+1, ... of this slot) filled by
+// TMA and issues every layer's tcgen05.mma chain for the slot's tiles; the
+// four slots' chains run in four warps, so their issue latencies overlap.
+// In the row-major ablation all 32 lanes also rebuild each layer's B operand
+// from the row-major weights into the slot's two B stages right before the
+// MMAs that read it.
 template <int V>
-__device__ __forceinline__ void run_producer(const FusedParams& p, const Ctx& c, int lane) {
-  const uint32_t R = p.n_in_stages;
+__device__ __forceinline__ void run_slot_control(const FusedParams& p, const Ctx& c, int32_t s,
+                                                 int lane) {
   const int32_t S = static_cast<int32_t>(p.n_slots);
-  int32_t last_round[kMaxInStages];
-#pragma unroll
-  for (int s = 0; s < kMaxInStages; ++s) last_round[s] = -1;
-
+  const uint32_t D = p.n_in_stages;  // input stages of this slot
+  const int L = p.L;
+  const int32_t n_rounds = (c.n_local - s + S - 1) / S;  // tiles r*S + s < n_local
+  int32_t issued = -1;  // last round whose input load was issued
   bool ok = true;
-  if (V == kVarRowMajor) ok = warp_wait(c.bar(kBarWLoad), 0, p, c);
-  uint32_t g = 0;
-  for (int32_t r = 0; r * S < c.n_local && ok; ++r) {
-    // Input tiles of this round, in tile order.
-    for (int32_t s = 0; s < S && ok; ++s) {
-      const int32_t i = r * S + s;
-      if (i >= c.n_local) break;
-      if (lane == 0) {
-        const uint32_t st = static_cast<uint32_t>(i) % R, rnd = static_cast<uint32_t>(i) / R;
-        ok = wait_phase(c.bar(kBarInEmpty + st), (rnd & 1u) ^ 1u, p.wait_ns, c.abort_flag, p.status);
-        if (ok) {
-          mbar_arrive_expect_tx(c.bar(kBarInFull + st), static_cast<uint32_t>(kTileM * 2 * p.d0));
-          issue_input_tma(p, c.sbase + p.sm_in + st * p.in_stage_bytes, c.bar(kBarInFull + st),
-                          tile_of(i));
-          last_round[st] = static_cast<int32_t>(rnd);
-        }
+  if (lane == 0) {
+    if (p.test_stall) ok = wait_phase(c.bar(kBarNever), 0, p.wait_ns, c.abort_flag, p.status);
+    if (ok) ok = wait_phase(c.bar(kBarWLoad), 0, p.wait_ns, c.abort_flag, p.status);
+  }
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  uint32_t g = 0;  // B stages used (row-major ablation)
+  for (int32_t r = 0; r < n_rounds && ok; ++r) {
+    if (lane == 0) {
+      // Keep the input ring D rounds ahead. A stage is free once the layer-1
+      // MMAs of the round that used it D rounds ago have completed.
+      while (ok && issued + 1 < r + static_cast<int32_t>(D) && issued + 1 < n_rounds) {
+        const uint32_t rr = static_cast<uint32_t>(issued + 1);
+        const uint32_t st = static_cast<uint32_t>(s) * D + rr % D;
+        ok = wait_phase(c.bar(kBarInEmpty + st), ((rr / D) & 1u) ^ 1u, p.wait_ns, c.abort_flag,
+                        p.status);
+        if (!ok) break;
+        mbar_arrive_expect_tx(c.bar(kBarInFull + st), static_cast<uint32_t>(kTileM * 2 * p.d0));
+        issue_input_tma(p, c.sbase + p.sm_in + st * p.in_stage_bytes, c.bar(kBarInFull + st),
+                        tile_of(static_cast<int32_t>(rr) * S + s));
+        issued = static_cast<int32_t>(rr);
       }
     }
-    if (V == kVarRowMajor) {
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      // Rebuild every layer's B operand for every tile of this round from the
-      // row-major weights, in the order the MMA thread consumes them:
-      // 16-byte row-major loads, swizzled 16-byte smem stores.
-      const Schedule* sc = c.sched(p);
-      for (int l = 0; l < p.L && ok; ++l) {
-        const int K = sc->layer[l].K, N = sc->layer[l].N, kc = K >> 3;
-        const uint16_t* Wl = p.mirror + sc->layer[l].rm_off;
-        for (int32_t s = 0; s < S && ok; ++s) {
-          if (r * S + s >= c.n_local) break;
-          const uint32_t bs = g % p.n_b_stages, brnd = g / p.n_b_stages;
-          ok = warp_wait(c.bar(kBarBEmpty + bs), (brnd & 1u) ^ 1u, p, c);
-          if (!ok) break;
-          const uint32_t stage = c.sbase + p.sm_b + bs * p.b_stage_bytes;
-          for (int idx = lane; idx < N * kc; idx += 32) {
-            const int n = idx / kc, col = (idx - n * kc) << 3;
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(Wl + n * K + col));
-            uint32_t off;
-            int w, k0;
-            locate(static_cast<uint32_t>(N), K, col, off, w, k0);
-            st_shared_v4(stage + off + swz(static_cast<uint32_t>(n * 2 * w + (col - k0) * 2), w),
-                         v.x, v.y, v.z, v.w);
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(r) % D;
+    for (int l = 0; l < L && ok; ++l) {
+      const LayerRegs li = load_layer(p, c, l);
+      uint32_t b_base = c.sbase + p.sm_w + li.w_off, bs = 0;
+      if (V == kVarRowMajor) {
+        // Rebuild W_l in one of this slot's two B stages from the row-major
+        // weights: 16-byte row-major loads, swizzled 16-byte smem stores.
+        bs = static_cast<uint32_t>(s) * 2u + (g & 1u);
+        ok = warp_wait(c.bar(kBarBEmpty + bs), ((g >> 1) & 1u) ^ 1u, p, c);
+        if (!ok) break;
+        b_base = c.sbase + p.sm_b + bs * p.b_stage_bytes;
+        const int K = li.K, N = li.N, kc = K >> 3;
+        const uint16_t* Wl = p.mirror + li.rm_off;
+        for (int idx = lane; idx < N * kc; idx += 32) {
+          const int n = idx / kc, col = (idx - n * kc) << 3;
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(Wl + n * K + col));
+          uint32_t off;
+          int w, k0;
+          locate(static_cast<uint32_t>(N), K, col, off, w, k0);
+          st_shared_v4(b_base + off + swz(static_cast<uint32_t>(n * 2 * w + (col - k0) * 2), w), v.x,
+                       v.y, v.z, v.w);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (lane == 0) {
+        const int32_t q = r * L + l - 1;  // completion of this slot's previous epilogue
+        if (q >= 0)
+          ok = wait_phase(c.bar(kBarActReady + s), static_cast<uint32_t>(q) & 1u, p.wait_ns,
+                          c.abort_flag, p.status);
+        if (ok && l == 0)
+          ok = wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(r) / D) & 1u, p.wait_ns,
+                          c.abort_flag, p.status);
+        if (ok) {
+          tc_fence_after_sync();
+          const uint64_t b_add = b_base >> 4;
+          const uint32_t slot_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
+          if (l == 0) {
+            // Layer 1: A is the input tile in shared memory.
+            const uint64_t a_add = (c.sbase + p.sm_in + st * p.in_stage_bytes) >> 4;
+            for (uint32_t j = li.slab_begin; j < li.slab_end; ++j) {
+              const uint4 sd = ld_shared_u32x4(c.slab_addr(p, j));
+              const uint64_t ad = (static_cast<uint64_t>(sd.y) << 32 | sd.x) + a_add;
+              const uint64_t bd = (static_cast<uint64_t>(sd.w) << 32 | sd.z) + b_add;
+              umma_f16_ss(slot_tmem, ad, bd, li.idesc, j > li.slab_begin ? 1u : 0u);
+            }
+          } else {
+            // Later layers: A is the previous epilogue's FP16 output in TMEM,
+            // 8 columns per 16-wide k-slab.
+            const uint32_t a_tmem = slot_tmem + p.a_col;
+            for (uint32_t j = li.slab_begin; j < li.slab_end; ++j) {
+              const uint4 sd = ld_shared_u32x4(c.slab_addr(p, j));
+              const uint64_t bd = (static_cast<uint64_t>(sd.w) << 32 | sd.z) + b_add;
+              umma_f16_ts(slot_tmem, a_tmem + 8u * (j - li.slab_begin), bd, li.idesc,
+                          j > li.slab_begin ? 1u : 0u);
+            }
           }
-          fence_proxy_async_smem();
-          mbar_arrive(c.bar(kBarBFull + bs));
-          ++g;
+          umma_commit(c.bar(kBarAccFull + s));
+          if (l == 0) umma_commit(c.bar(kBarInEmpty + st));
+          if (V == kVarRowMajor) umma_commit(c.bar(kBarBEmpty + bs));
         }
       }
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      ++g;
     }
   }
   if (lane == 0) {
-    // Drain: every copy this warp issued (input tiles, the one-time weight and
-    // schedule staging) must land before the CTA may exit.
-    for (uint32_t s = 0; s < R; ++s)
-      if (last_round[s] >= 0) wait_drain(c.bar(kBarInFull + s), last_round[s] & 1, p.status);
-    wait_drain(c.bar(kBarWLoad), 0, p.status);
-  }
-}
-
-// ------------------------------------------------------------------ MMA issuer
-template <int V>
-__device__ __forceinline__ void run_mma(const FusedParams& p, const Ctx& c) {
-  const uint32_t R = p.n_in_stages;
-  const int32_t S = static_cast<int32_t>(p.n_slots);
-  const int L = p.L;
-  bool ok = true;
-  if (p.test_stall) ok = wait_phase(c.bar(kBarNever), 0, p.wait_ns, c.abort_flag, p.status);
-  if (ok) ok = wait_phase(c.bar(kBarWLoad), 0, p.wait_ns, c.abort_flag, p.status);
-  const Schedule* sc = c.sched(p);
-  uint32_t g = 0;
-  for (int32_t r = 0; r * S < c.n_local && ok; ++r) {
-    for (int l = 0; l < L && ok; ++l) {
-      const uint32_t sb = sc->layer[l].slab_begin, se = sc->layer[l].slab_end;
-      const uint32_t idesc = sc->layer[l].idesc;
-      const uint32_t w_base = c.sbase + p.sm_w + sc->layer[l].w_off;
-      for (int32_t s = 0; s < S; ++s) {
-        const int32_t i = r * S + s;
-        if (i >= c.n_local) break;
-        const uint32_t st = static_cast<uint32_t>(i) % R;
-        const int32_t q = r * L + l - 1;  // completion of this slot's previous epilogue
-        if (q >= 0 && !wait_phase(c.bar(kBarActReady + s), static_cast<uint32_t>(q) & 1u, p.wait_ns,
-                                  c.abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
-        if (l == 0 && !wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(i) / R) & 1u,
-                                  p.wait_ns, c.abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
-        uint32_t b_base = w_base, bs = 0;
-        if (V == kVarRowMajor) {
-          bs = g % p.n_b_stages;
-          if (!wait_phase(c.bar(kBarBFull + bs), (g / p.n_b_stages) & 1u, p.wait_ns, c.abort_flag,
-                          p.status)) {
-            ok = false;
-            break;
-          }
-          b_base = c.sbase + p.sm_b + bs * p.b_stage_bytes;
-        }
-        tc_fence_after_sync();
-        const uint32_t a_base =
-            (l == 0) ? (c.sbase + p.sm_in + st * p.in_stage_bytes)
-                     : (c.sbase + p.sm_act + static_cast<uint32_t>(s) * p.act_slot_bytes);
-        const uint64_t a_add = a_base >> 4, b_add = b_base >> 4;
-        const uint32_t d_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
-        for (uint32_t j = sb; j < se; ++j) {
-          const SlabDesc sd = sc->slab[j];
-          umma_f16_ss(d_tmem, sd.a + a_add, sd.b + b_add, idesc, j > sb ? 1u : 0u);
-        }
-        umma_commit(c.bar(kBarAccFull + s));
-        if (l == 0) umma_commit(c.bar(kBarInEmpty + st));
-        if (V == kVarRowMajor) {
-          umma_commit(c.bar(kBarBEmpty + bs));
-          ++g;
-        }
-      }
+    // Drain: every MMA this thread issued completes, and every input load it
+    // issued lands, before the CTA may exit.
+    umma_commit(c.bar(kBarDrain + s));
+    wait_drain(c.bar(kBarDrain + s), 0, p.status);
+    for (int32_t rr = (issued - static_cast<int32_t>(D) + 1 > 0 ? issued - static_cast<int32_t>(D) + 1 : 0);
+         rr <= issued; ++rr) {
+      const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(rr) % D;
+      wait_drain(c.bar(kBarInFull + st), (static_cast<uint32_t>(rr) / D) & 1u, p.status);
     }
   }
-  // Drain: all MMAs issued by this thread complete before teardown.
-  umma_commit(c.bar(kBarDrain));
-  wait_drain(c.bar(kBarDrain), 0, p.status);
 }
 
 // ------------------------------------------------------------------ epilogue
@@ -300,6 +324,37 @@ __device__ __forceinline__ uint32_t out_chunk_off(int c0) {
   return static_cast<uint32_t>(c0 >> 5) * (kTileM * 64u);
 }
 
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, int w, uint32_t (&acc)[32]) {
+  if (w == 32)
+    tmem_ld_x32(taddr, acc);
+  else
+    tmem_ld_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(acc));
+}
+
+// Bias, rounding and activation of one chunk of w columns starting at c0,
+// then its stores: FP16 pairs into the slot's A region in TMEM (columns
+// c0/2 ..), or, after the last layer, 16-byte stores into the output staging
+// region of the chunk.
+template <int V>
+__device__ __forceinline__ void epilogue_store(const uint32_t (&acc)[32], int c0, int w,
+                                               uint32_t bias_addr, bool last, __half2 slope2,
+                                               uint32_t row, uint32_t out_dst, uint32_t a_tmem) {
+  uint32_t h[16];
+  epilogue_chunk<V>(acc, bias_addr + 4u * static_cast<uint32_t>(c0), w >> 1, !last, slope2, h);
+  if (last) {
+    const uint32_t base = out_dst + out_chunk_off(c0);
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc)
+      if (cc * 8 < w)
+        st_shared_v4_nc(base + swz(row * 2u * static_cast<uint32_t>(w) + cc * 16u, w), h[4 * cc],
+                        h[4 * cc + 1], h[4 * cc + 2], h[4 * cc + 3]);
+  } else if (w == 32) {
+    tmem_st_x16(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
+  } else {
+    tmem_st_x8(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
+  }
+}
+
 // Epilogue warp e serves tile slot e / (4G), column group (e % 4G) / 4 and
 // TMEM lane quadrant (warp index % 4), where G = 16 / (4 * slots) column
 // groups share the columns of a layer in 32-column chunks g, g + G, ...
@@ -308,20 +363,17 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
                                              int lane) {
   const int32_t S = static_cast<int32_t>(p.n_slots);
   const int G = kEpiWarps / (4 * S);
-  const int e = warp - 2;
+  const int e = warp - kCtrlWarps;
   const int32_t s = e / (4 * G);
   const int g = (e % (4 * G)) / 4;
   const int quad = warp & 3;  // TMEM lane quadrant this warp may access
   const uint32_t row = static_cast<uint32_t>(quad * 32 + lane);
   const uint32_t lane_bits = static_cast<uint32_t>(quad * 32) << 16;
   const __half2 slope2 = __float2half2_rn(0.01f);  // half(0.01)
-  const float* sbias = reinterpret_cast<const float*>(c.gbase + p.sm_bias);
   const int L = p.L;
   const int n_out = p.dL;
   const bool storer = (lane == 0) && (32 * g < n_out);
   if (!warp_wait(c.bar(kBarWLoad), 0, p, c)) return;
-  const Schedule* sc = c.sched(p);
-  const uint32_t act_dst = c.sbase + p.sm_act + static_cast<uint32_t>(s) * p.act_slot_bytes;
   const uint32_t tbase = c.tmem + lane_bits + static_cast<uint32_t>(s) * p.slot_cols;
   for (int32_t r = 0; r * S + s < c.n_local; ++r) {
     const int32_t t = tile_of(r * S + s);
@@ -333,9 +385,10 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
         break;
       }
       tc_fence_after_sync();
-      const int N = sc->layer[l].N;
+      const LayerRegs li = load_layer(p, c, l);
+      const int N = li.N;
       const bool last = (l == L - 1);
-      const float* bias = sbias + sc->layer[l].bias_f_off;
+      const uint32_t bias_addr = c.sbase + p.sm_bias + 4u * li.bias_f_off;
       const uint32_t out_dst =
           c.sbase + p.sm_out +
           (static_cast<uint32_t>(s) * p.n_out_bufs + static_cast<uint32_t>(r) % p.n_out_bufs) *
@@ -351,40 +404,17 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
         }
         __syncwarp();
       }
+      // Chunks of this warp are 32 columns wide (a trailing one may be 16).
       for (int c0 = 32 * g; c0 < N; c0 += 32 * G) {
+        const int w0 = (N - c0 >= 32) ? 32 : 16;
         uint32_t acc[32];
-        uint32_t h[16];
-        const int cols = (N - c0 >= 32) ? 32 : 16;
-        if (cols == 32) {
-          tmem_ld_x32(tbase + static_cast<uint32_t>(c0), acc);
-        } else {
-          tmem_ld_x16(tbase + static_cast<uint32_t>(c0), *reinterpret_cast<uint32_t(*)[16]>(acc));
-        }
+        tmem_ld_cols(tbase + static_cast<uint32_t>(c0), w0, acc);
         tmem_wait_ld();
-        epilogue_chunk<V>(acc, bias + c0, cols >> 1, !last, slope2, h);
-        if (last) {
-          const uint32_t base = out_dst + out_chunk_off(c0);
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-            if (cc * 8 < cols)
-              st_shared_v4_nc(base + swz(row * 2u * static_cast<uint32_t>(cols) + cc * 16u, cols),
-                              h[4 * cc], h[4 * cc + 1], h[4 * cc + 2], h[4 * cc + 3]);
-        } else {
-          uint32_t off;
-          int w, k0;
-          locate(kTileM, N, c0, off, w, k0);  // a 32-column chunk never straddles segments
-          const uint32_t base = act_dst + off;
-          const uint32_t lin0 =
-              row * 2u * static_cast<uint32_t>(w) + static_cast<uint32_t>(c0 - k0) * 2u;
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-            if (cc * 8 < cols)
-              st_shared_v4_nc(base + swz(lin0 + cc * 16u, w), h[4 * cc], h[4 * cc + 1],
-                              h[4 * cc + 2], h[4 * cc + 3]);
-        }
+        epilogue_store<V>(acc, c0, w0, bias_addr, last, slope2, row, out_dst, tbase + p.a_col);
       }
+      if (!last) tmem_wait_st();
       tc_fence_before_sync();
-      fence_proxy_async_smem();
+      if (last) fence_proxy_async_smem();  // staging tile -> TMA store (async proxy)
       mbar_arrive(c.bar(kBarActReady + s));
       if (last) {
         __syncwarp();
@@ -434,13 +464,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     for (int s = 0; s < kMaxSlots; ++s) {
       mbar_init(c.bar(kBarAccFull + s), 1);
       mbar_init(c.bar(kBarActReady + s), epi_per_slot);
+      mbar_init(c.bar(kBarDrain + s), 1);
     }
-    for (int s = 0; s < kMaxBStages; ++s) {
-      mbar_init(c.bar(kBarBFull + s), 32);
-      mbar_init(c.bar(kBarBEmpty + s), 1);
-    }
+    for (int s = 0; s < kMaxBStages; ++s) mbar_init(c.bar(kBarBEmpty + s), 1);
     mbar_init(c.bar(kBarWLoad), 1);
-    mbar_init(c.bar(kBarDrain), 1);
     mbar_init(c.bar(kBarNever), 1);
     *c.abort_flag = 0u;
     fence_mbar_init();
@@ -460,22 +487,20 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   tc_fence_after_sync();
   c.tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // Stage the schedule (and the packed weight images) once for the whole
-      // persistent loop.
-      const uint32_t wbytes = (V == kVarRowMajor) ? 0u : p.bias_off;
-      mbar_arrive_expect_tx(c.bar(kBarWLoad), p.sched_bytes + wbytes);
-      bulk_load(c.sbase + p.sm_sched, p.sched, p.sched_bytes, c.bar(kBarWLoad));
-      for (uint32_t off = 0; off < wbytes; off += 32768u) {
-        const uint32_t bytes = (wbytes - off) < 32768u ? (wbytes - off) : 32768u;
-        bulk_load(c.sbase + p.sm_w + off, p.blob + off, bytes, c.bar(kBarWLoad));
-      }
+  if (warp == 0 && lane == 0) {
+    // Stage the schedule (and the packed weight images) once for the whole
+    // persistent loop.
+    const uint32_t wbytes = (V == kVarRowMajor) ? 0u : p.bias_off;
+    mbar_arrive_expect_tx(c.bar(kBarWLoad), p.sched_bytes + wbytes);
+    bulk_load(c.sbase + p.sm_sched, p.sched, p.sched_bytes, c.bar(kBarWLoad));
+    for (uint32_t off = 0; off < wbytes; off += 32768u) {
+      const uint32_t bytes = (wbytes - off) < 32768u ? (wbytes - off) : 32768u;
+      bulk_load(c.sbase + p.sm_w + off, p.blob + off, bytes, c.bar(kBarWLoad));
     }
-    if (V == kVarRowMajor || lane == 0) run_producer<V>(p, c, lane);
-  } else if (warp == 1) {
-    if (lane == 0) run_mma<V>(p, c);
-    __syncwarp();
+  }
+  if (warp < kCtrlWarps) {
+    if (warp < static_cast<int>(p.n_slots)) run_slot_control<V>(p, c, warp, lane);
+    if (warp == 0 && lane == 0) wait_drain(c.bar(kBarWLoad), 0, p.status);
   } else {
     run_epilogue<V>(p, c, warp, lane);
   }
@@ -536,50 +561,50 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
   p.n_bias = nb;
   p.d0 = dims[0];
   p.dL = dims[L];
-  uint32_t slot = 32;  // TMEM columns per slot: the widest layer, as a power of two
-  while (slot < nmax) slot <<= 1;
-  p.slot_cols = slot;
-
-  p.act_slot_bytes = align1024(image_bytes(kTileM, static_cast<int>(act_w)));
+  // TMEM per slot: the accumulator (widest layer) then the A region (half the
+  // widest hidden layer, two FP16 values per column), each a multiple of 32.
+  const uint32_t acc_cols = (nmax + 31u) & ~31u;
+  const uint32_t a_cols = ((act_w / 2u) + 31u) & ~31u;
+  p.a_col = acc_cols;
+  p.slot_cols = acc_cols + a_cols;
   // output staging: 8 KB per 32-column chunk, 4 KB for a trailing 16-column one
   p.out_slot_bytes = static_cast<uint32_t>(p.dL >> 5) * (kTileM * 64u) +
                      ((p.dL & 31) ? kTileM * 32u : 0u);
   p.b_stage_bytes = (variant == kVarRowMajor) ? align1024(bstage) : 0u;
-  p.n_b_stages = (variant == kVarRowMajor) ? kMaxBStages : 0u;
   const uint32_t stage = align1024(image_bytes(kTileM, p.d0));
 
-  // Most tile slots first (4, 2, 1) as TMEM allows, then two output buffers
-  // before one, then the deepest input ring (4 down to 2) that fits.
+  // Most tile slots first (4, 2, 1) as TMEM allows, then two input stages
+  // per slot before one, then two output buffers per slot before one.
   for (uint32_t slots = kMaxSlots; slots >= 1; slots >>= 1) {
-    if (slots * slot > 512u) continue;
-    for (uint32_t obufs = kOutBufs; obufs >= 1; --obufs) {
-      uint32_t off = 0;
-      p.sm_w = 0;
-      off += (variant == kVarRowMajor) ? 0u : align1024(p.bias_off);
-      p.sm_sched = off;
-      off += align1024(p.sched_bytes);
-      p.sm_bias = off;
-      off += align1024(nb * 4u);
-      p.sm_act = off;
-      off += slots * p.act_slot_bytes;
-      p.sm_out = off;
-      off += slots * obufs * p.out_slot_bytes;
-      p.sm_b = off;
-      off += p.n_b_stages * p.b_stage_bytes;
-      p.sm_bar = off;
-      off += 1024u;  // barrier block, keeps the input ring 1024-aligned
-      p.sm_in = off;
-      const uint32_t fixed = off + 1024u;  // + alignment slack of the dynamic smem base
-      for (uint32_t stages = kMaxInStages; stages >= 2; --stages) {
-        if (fixed + stages * stage <= smem_optin) {
+    if (slots * p.slot_cols > 512u) continue;
+    p.n_b_stages = (variant == kVarRowMajor) ? 2u * slots : 0u;
+    for (uint32_t depth = 2; depth >= 1; --depth) {
+      for (uint32_t obufs = kOutBufs; obufs >= 1; --obufs) {
+        uint32_t off = 0;
+        p.sm_w = 0;
+        off += (variant == kVarRowMajor) ? 0u : align1024(p.bias_off);
+        p.sm_sched = off;
+        off += align1024(p.sched_bytes);
+        p.sm_bias = off;
+        off += align1024(nb * 4u);
+        p.sm_out = off;
+        off += slots * obufs * p.out_slot_bytes;
+        p.sm_b = off;
+        off += p.n_b_stages * p.b_stage_bytes;
+        p.sm_bar = off;
+        off += 1024u;  // barrier block, keeps the input ring 1024-aligned
+        p.sm_in = off;
+        off += slots * depth * stage;
+        const uint32_t total = off + 1024u;  // + alignment slack of the dynamic smem base
+        if (total <= smem_optin) {
           uint32_t cols = 32;
-          while (cols < slots * slot) cols <<= 1;
+          while (cols < slots * p.slot_cols) cols <<= 1;
           p.tmem_cols = cols;
           p.n_slots = slots;
           p.in_stage_bytes = stage;
-          p.n_in_stages = stages;
+          p.n_in_stages = depth;
           p.n_out_bufs = obufs;
-          return fixed + stages * stage;
+          return total;
         }
       }
     }

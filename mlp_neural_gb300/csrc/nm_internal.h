@@ -12,32 +12,32 @@
 namespace nm {
 
 constexpr int kMaxSlots = 4;       // 128-sample tiles in flight per CTA (upper bound)
-constexpr int kMaxInStages = 4;    // input TMA ring depth (upper bound)
-constexpr int kMaxBStages = 4;     // B-operand ring depth of the row-major ablation
+constexpr int kMaxInStages = 2 * kMaxSlots;  // input TMA ring: up to 2 stages per slot
+constexpr int kMaxBStages = 2 * kMaxSlots;   // row-major ablation: 2 B stages per slot
+constexpr int kCtrlWarps = kMaxSlots;        // one control warp (MMA issue + input TMA) per slot
 constexpr int kEpiWarps = 16;      // epilogue warps: slots x 4 lane quadrants x column groups
-// warp 0 producer, warp 1 MMA issuer, then the epilogue warps
-constexpr int kFusedThreads = 64 + 32 * kEpiWarps;
+constexpr int kFusedThreads = 32 * (kCtrlWarps + kEpiWarps);
 constexpr int kOutBufs = 2;        // output staging buffers per slot (TMA-store double buffer)
 constexpr int kMaxSlabs = kMaxLayers * (kMaxDim / 16);
 constexpr uint32_t kStatusTimeout = 1u;
 
 enum Variant : int { kVarFused = 0, kVarRowMajor = 1, kVarScalar = 2 };
 
-// Barrier slots inside the barrier block of the fused kernel's smem.
+// Barrier slots inside the barrier block of the fused kernel's smem. Input
+// stage s * n_in_stages + k belongs to slot s; likewise B stages 2s, 2s + 1.
 enum BarIndex : int {
   kBarInFull = 0,
   kBarInEmpty = kBarInFull + kMaxInStages,
   kBarAccFull = kBarInEmpty + kMaxInStages,
   kBarActReady = kBarAccFull + kMaxSlots,
-  kBarBFull = kBarActReady + kMaxSlots,
-  kBarBEmpty = kBarBFull + kMaxBStages,
+  kBarBEmpty = kBarActReady + kMaxSlots,
   kBarWLoad = kBarBEmpty + kMaxBStages,
-  kBarDrain = kBarWLoad + 1,
-  kBarNever = kBarDrain + 1,  // never signalled (failure-path test hook)
+  kBarDrain = kBarWLoad + 1,  // one per slot
+  kBarNever = kBarDrain + kMaxSlots,  // never signalled (failure-path test hook)
   kBarCount = kBarNever + 1
 };
-constexpr uint32_t kTmemSlotOff = 256;  // barriers first, then the TMEM address and abort flag
-constexpr uint32_t kAbortOff = 260;
+constexpr uint32_t kTmemSlotOff = 512;  // barriers first, then the TMEM address and abort flag
+constexpr uint32_t kAbortOff = 516;
 static_assert(kBarCount * 8 <= kTmemSlotOff, "barrier block overflow");
 
 // Per-layer schedule entry (host-built, copied to smem once per CTA).
@@ -86,12 +86,14 @@ struct FusedParams {  // 128-byte aligned through its CUtensorMap members
   uint32_t n_bias;        // sum of d_1..d_L
   uint32_t sched_bytes;   // bytes of the schedule to copy
   // shared-memory plan (byte offsets from the 1024-aligned base)
-  uint32_t sm_w, sm_sched, sm_bias, sm_in, sm_act, sm_out, sm_b, sm_bar;
-  uint32_t in_stage_bytes, act_slot_bytes, out_slot_bytes, b_stage_bytes;
-  uint32_t n_in_stages, n_b_stages, n_out_bufs;
+  uint32_t sm_w, sm_sched, sm_bias, sm_in, sm_out, sm_b, sm_bar;
+  uint32_t in_stage_bytes, out_slot_bytes, b_stage_bytes;
+  uint32_t n_in_stages;  // input stages per slot
+  uint32_t n_b_stages, n_out_bufs;
   uint32_t n_slots;     // tiles in flight (1, 2 or 4); kEpiWarps / (4 * n_slots) column groups
   uint32_t tmem_cols;   // allocated TMEM columns (power of two)
-  uint32_t slot_cols;   // TMEM columns per tile slot
+  uint32_t slot_cols;   // TMEM columns per tile slot: accumulator, then the A region
+  uint32_t a_col;       // column of the A region (next layer's FP16 activations) in a slot
   uint64_t wait_ns;     // limit of every pipeline wait
   uint32_t test_stall;  // non-zero: the MMA thread first waits on kBarNever
 };
