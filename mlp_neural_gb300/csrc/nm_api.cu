@@ -274,7 +274,16 @@ nm_status nm_mlp_create(const int32_t* dims, int32_t n_dims, nm_mlp** out) {
     delete h;
     return NM_ERR_OOM;
   }
-  p.sched_bytes = nm::build_schedule(h->dims, L, h->w_off, h->rm_off, *sc);
+  p.sched_bytes = nm::build_schedule(h->dims, L, h->w_off, h->rm_off, *sc, &p.bslab_bytes);
+  {
+    uint32_t row0 = 0;
+    for (int l = 0; l < L; ++l) {
+      p.bias_row0[l] = row0;
+      p.bslab_off[l] = sc->layer[l].bslab_off;
+      row0 += static_cast<uint32_t>(dims[l + 1]);
+    }
+    p.n_bias = row0;
+  }
 
   if (cudaMalloc(&h->blob, h->blob_size) != cudaSuccess) {
     delete sc;

@@ -76,7 +76,7 @@ struct Ctx {
 // LayerInfo as loaded from shared memory (two 16-byte loads).
 struct LayerRegs {
   int32_t K, N;
-  uint32_t slab_begin, slab_end, idesc, bias_f_off, rm_off, w_off;
+  uint32_t slab_begin, slab_end, idesc, bslab_off, rm_off, w_off;
 };
 
 __device__ __forceinline__ LayerRegs load_layer(const FusedParams& p, const Ctx& c, int l) {
@@ -88,7 +88,7 @@ __device__ __forceinline__ LayerRegs load_layer(const FusedParams& p, const Ctx&
   r.slab_begin = x.z;
   r.slab_end = x.w;
   r.idesc = y.x;
-  r.bias_f_off = y.y;
+  r.bslab_off = y.y;
   r.rm_off = y.z;
   r.w_off = y.w;
   return r;
@@ -117,6 +117,32 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, uint64
   return wait_phase_slow(bar, parity, limit_ns, abort_flag, status);
 }
 
+// Bounded wait by busy polling with test_wait: no suspend/wake-up latency.
+// Used by the single issuing thread of a control warp, where reacting fast
+// to the epilogue's arrival is on the critical path.
+__device__ __noinline__ bool spin_phase_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                             volatile uint32_t* abort_flag, uint32_t* status) {
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((++spins & 255u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        *abort_flag = 1u;
+        atomicOr(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool spin_phase(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                           volatile uint32_t* abort_flag, uint32_t* status) {
+  if (mbar_test_wait(bar, parity)) return true;
+  return spin_phase_slow(bar, parity, limit_ns, abort_flag, status);
+}
+
 // Wait used while draining: ignores the abort flag, fixed limit.
 __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, uint32_t* status) {
   const uint64_t t0 = globaltimer_ns();
@@ -135,20 +161,16 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const F
   return __all_sync(0xFFFFFFFFu, got);
 }
 
-// FP32 accumulator pairs + FP32 bias -> FP16 pairs (round to nearest even),
-// then the activation when `act` is set. Column 2j goes to the low half.
+// FP32 accumulator pairs (bias already added by the tensor core) -> FP16
+// pairs (round to nearest even), then the activation when `act` is set.
+// Column 2j goes to the low half.
 template <int V>
-__device__ __forceinline__ void epilogue_chunk(const uint32_t* acc, uint32_t bias_addr, int npairs,
-                                               bool act, __half2 slope2, uint32_t* out) {
+__device__ __forceinline__ void epilogue_chunk(const uint32_t* acc, int npairs, bool act,
+                                               __half2 slope2, uint32_t* out) {
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     if (j < npairs) {
-      const float2 a = make_float2(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
-      // one 16-byte broadcast load serves two pairs
-      const float4 b4 = ld_shared_f32x4(bias_addr + 16u * static_cast<uint32_t>(j >> 1));
-      const float2 b = (j & 1) ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
-      const float2 v = __fadd2_rn(a, b);
-      __half2 h = __float22half2_rn(v);
+      __half2 h = __floats2half2_rn(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
       if (V != kVarScalar) {
         if (act) h = __hmax2(h, __hmul2(h, slope2));
       }
@@ -261,9 +283,14 @@ __device__ __forceinline__ void run_slot_control(const FusedParams& p, const Ctx
         __syncwarp();
       }
       if (lane == 0) {
+        // Descriptors of the first k-slabs, fetched before the wait.
+        uint4 pre[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (li.slab_begin + k < li.slab_end) pre[k] = ld_shared_u32x4(c.slab_addr(p, li.slab_begin + k));
         const int32_t q = r * L + l - 1;  // completion of this slot's previous epilogue
         if (q >= 0)
-          ok = wait_phase(c.bar(kBarActReady + s), static_cast<uint32_t>(q) & 1u, p.wait_ns,
+          ok = spin_phase(c.bar(kBarActReady + s), static_cast<uint32_t>(q) & 1u, p.wait_ns,
                           c.abort_flag, p.status);
         if (ok && l == 0)
           ok = wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(r) / D) & 1u, p.wait_ns,
@@ -272,26 +299,38 @@ __device__ __forceinline__ void run_slot_control(const FusedParams& p, const Ctx
           tc_fence_after_sync();
           const uint64_t b_add = b_base >> 4;
           const uint32_t slot_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
-          if (l == 0) {
-            // Layer 1: A is the input tile in shared memory.
-            const uint64_t a_add = (c.sbase + p.sm_in + st * p.in_stage_bytes) >> 4;
-            for (uint32_t j = li.slab_begin; j < li.slab_end; ++j) {
-              const uint4 sd = ld_shared_u32x4(c.slab_addr(p, j));
-              const uint64_t ad = (static_cast<uint64_t>(sd.y) << 32 | sd.x) + a_add;
-              const uint64_t bd = (static_cast<uint64_t>(sd.w) << 32 | sd.z) + b_add;
-              umma_f16_ss(slot_tmem, ad, bd, li.idesc, j > li.slab_begin ? 1u : 0u);
-            }
-          } else {
-            // Later layers: A is the previous epilogue's FP16 output in TMEM,
-            // 8 columns per 16-wide k-slab.
-            const uint32_t a_tmem = slot_tmem + p.a_col;
-            for (uint32_t j = li.slab_begin; j < li.slab_end; ++j) {
-              const uint4 sd = ld_shared_u32x4(c.slab_addr(p, j));
-              const uint64_t bd = (static_cast<uint64_t>(sd.w) << 32 | sd.z) + b_add;
-              umma_f16_ts(slot_tmem, a_tmem + 8u * (j - li.slab_begin), bd, li.idesc,
-                          j > li.slab_begin ? 1u : 0u);
+          // Layer 1 reads A (the input tile) from shared memory; later layers
+          // read the previous epilogue's FP16 output from TMEM, 8 columns per
+          // 16-wide k-slab.
+          const uint64_t a_add =
+              (l == 0) ? static_cast<uint64_t>((c.sbase + p.sm_in + st * p.in_stage_bytes) >> 4) : 0ull;
+          const uint32_t a_tmem = slot_tmem + p.a_col;
+          const uint32_t nslab = li.slab_end - li.slab_begin;
+#pragma unroll
+          for (uint32_t k = 0; k < 4; ++k) {
+            if (k < nslab) {
+              const uint64_t bd = (static_cast<uint64_t>(pre[k].w) << 32 | pre[k].z) + b_add;
+              if (l == 0)
+                umma_f16_ss(slot_tmem, (static_cast<uint64_t>(pre[k].y) << 32 | pre[k].x) + a_add, bd,
+                            li.idesc, k > 0 ? 1u : 0u);
+              else
+                umma_f16_ts(slot_tmem, a_tmem + 8u * k, bd, li.idesc, k > 0 ? 1u : 0u);
             }
           }
+          for (uint32_t k = 4; k < nslab; ++k) {
+            const uint4 sd = ld_shared_u32x4(c.slab_addr(p, li.slab_begin + k));
+            const uint64_t bd = (static_cast<uint64_t>(sd.w) << 32 | sd.z) + b_add;
+            if (l == 0)
+              umma_f16_ss(slot_tmem, (static_cast<uint64_t>(sd.y) << 32 | sd.x) + a_add, bd, li.idesc, 1u);
+            else
+              umma_f16_ts(slot_tmem, a_tmem + 8u * k, bd, li.idesc, 1u);
+          }
+          // Bias: one more K=16 MMA, ones column x bias slab, added last.
+          const uint64_t bias_bd = smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u);
+          if (l == 0)
+            umma_f16_ss(slot_tmem, smem_desc(c.sbase + p.sm_ones, 256u, 6u), bias_bd, li.idesc, 1u);
+          else
+            umma_f16_ts(slot_tmem, slot_tmem + p.a_ones, bias_bd, li.idesc, 1u);
           umma_commit(c.bar(kBarAccFull + s));
           if (l == 0) umma_commit(c.bar(kBarInEmpty + st));
           if (V == kVarRowMajor) umma_commit(c.bar(kBarBEmpty + bs));
@@ -336,11 +375,11 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, int w, uint32_t (&a
 // c0/2 ..), or, after the last layer, 16-byte stores into the output staging
 // region of the chunk.
 template <int V>
-__device__ __forceinline__ void epilogue_store(const uint32_t (&acc)[32], int c0, int w,
-                                               uint32_t bias_addr, bool last, __half2 slope2,
-                                               uint32_t row, uint32_t out_dst, uint32_t a_tmem) {
+__device__ __forceinline__ void epilogue_store(const uint32_t (&acc)[32], int c0, int w, bool last,
+                                               __half2 slope2, uint32_t row, uint32_t out_dst,
+                                               uint32_t a_tmem) {
   uint32_t h[16];
-  epilogue_chunk<V>(acc, bias_addr + 4u * static_cast<uint32_t>(c0), w >> 1, !last, slope2, h);
+  epilogue_chunk<V>(acc, w >> 1, !last, slope2, h);
   if (last) {
     const uint32_t base = out_dst + out_chunk_off(c0);
 #pragma unroll
@@ -374,6 +413,13 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
   const int n_out = p.dL;
   const bool storer = (lane == 0) && (32 * g < n_out);
   if (!warp_wait(c.bar(kBarWLoad), 0, p, c)) return;
+  if (g == 0) {
+    // The constant A slab of the bias MMA for layers read from TMEM: column 0
+    // of every row holds (1.0, 0) as an FP16 pair, columns 1..7 zeros.
+    const uint32_t ones[8] = {0x3C00u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    tmem_st_x8(c.tmem + lane_bits + static_cast<uint32_t>(s) * p.slot_cols + p.a_ones, ones);
+    tmem_wait_st();
+  }
   const uint32_t tbase = c.tmem + lane_bits + static_cast<uint32_t>(s) * p.slot_cols;
   for (int32_t r = 0; r * S + s < c.n_local; ++r) {
     const int32_t t = tile_of(r * S + s);
@@ -388,7 +434,6 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
       const LayerRegs li = load_layer(p, c, l);
       const int N = li.N;
       const bool last = (l == L - 1);
-      const uint32_t bias_addr = c.sbase + p.sm_bias + 4u * li.bias_f_off;
       const uint32_t out_dst =
           c.sbase + p.sm_out +
           (static_cast<uint32_t>(s) * p.n_out_bufs + static_cast<uint32_t>(r) % p.n_out_bufs) *
@@ -410,7 +455,7 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
         uint32_t acc[32];
         tmem_ld_cols(tbase + static_cast<uint32_t>(c0), w0, acc);
         tmem_wait_ld();
-        epilogue_store<V>(acc, c0, w0, bias_addr, last, slope2, row, out_dst, tbase + p.a_col);
+        epilogue_store<V>(acc, c0, w0, last, slope2, row, out_dst, tbase + p.a_col);
       }
       if (!last) tmem_wait_st();
       tc_fence_before_sync();
@@ -477,10 +522,30 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     tmem_relinquish();
   }
   {
-    // FP16 biases of every layer -> FP32 in shared memory (exact widening).
-    float* sbias = reinterpret_cast<float*>(c.gbase + p.sm_bias);
-    const __half* gb = reinterpret_cast<const __half*>(p.blob + p.bias_off);
-    for (uint32_t j = threadIdx.x; j < p.n_bias; j += kFusedThreads) sbias[j] = __half2float(gb[j]);
+    // Ones tile (A of the layer-1 bias MMA) and the bias slabs (B of every
+    // layer's bias MMA), 32-byte-swizzle K-major: row r's first 16-byte chunk
+    // holds (value, 0 x 7) FP16, its second chunk zeros. Bias row j of the
+    // concatenated biases is row j - bias_row0[l] of layer l's slab.
+    const uint16_t* gb = reinterpret_cast<const uint16_t*>(p.blob + p.bias_off);
+    const uint32_t total_rows = kTileM + p.n_bias;
+    for (uint32_t idx = threadIdx.x; idx < 2u * total_rows; idx += kFusedThreads) {
+      const uint32_t rr = idx >> 1, ch = idx & 1u;
+      uint32_t base, row, v;
+      if (rr < kTileM) {
+        base = c.sbase + p.sm_ones;
+        row = rr;
+        v = 0x3C00u;
+      } else {
+        const uint32_t j = rr - kTileM;
+        int l = 0;
+        while (l + 1 < p.L && j >= p.bias_row0[l + 1]) ++l;
+        base = c.sbase + p.sm_bslab + p.bslab_off[l];
+        row = j - p.bias_row0[l];
+        v = gb[j];
+      }
+      st_shared_v4(base + swz(row * 32u + ch * 16u, 16), ch ? 0u : v, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -517,9 +582,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 
 // ------------------------------------------------------------------ host side
 uint32_t build_schedule(const int32_t* dims, int L, const uint32_t* w_off, const uint32_t* rm_off,
-                        Schedule& sc) {
+                        Schedule& sc, uint32_t* bslab_bytes) {
   std::memset(&sc, 0, sizeof(sc));
-  uint32_t slab = 0, nb = 0;
+  uint32_t slab = 0, boff = 0;
   for (int l = 0; l < L; ++l) {
     const int K = dims[l], N = dims[l + 1];
     LayerInfo& li = sc.layer[l];
@@ -527,23 +592,24 @@ uint32_t build_schedule(const int32_t* dims, int L, const uint32_t* w_off, const
     li.N = N;
     li.slab_begin = slab;
     li.idesc = idesc_f16_f32(kTileM, static_cast<uint32_t>(N));
-    li.bias_f_off = nb;
+    li.bslab_off = boff;
     li.rm_off = rm_off[l];
     li.w_off = w_off[l];
     for (int k = 0; k < K; k += 16) {
-      uint32_t aoff, boff;
+      uint32_t aoff, boff_w;
       int w, k0;
       locate(kTileM, K, k, aoff, w, k0);
-      locate(static_cast<uint32_t>(N), K, k, boff, w, k0);
+      locate(static_cast<uint32_t>(N), K, k, boff_w, w, k0);
       const uint32_t kb = static_cast<uint32_t>(k - k0) * 2u;
       const uint32_t sbo = 16u * static_cast<uint32_t>(w);
       sc.slab[slab].a = smem_desc(aoff + kb, sbo, swizzle_code(w));
-      sc.slab[slab].b = smem_desc(boff + kb, sbo, swizzle_code(w));
+      sc.slab[slab].b = smem_desc(boff_w + kb, sbo, swizzle_code(w));
       ++slab;
     }
     li.slab_end = slab;
-    nb += static_cast<uint32_t>(N);
+    boff += align1024(static_cast<uint32_t>(N) * 32u);
   }
+  *bslab_bytes = boff;
   return static_cast<uint32_t>(sizeof(LayerInfo) * kMaxLayers + sizeof(SlabDesc) * slab);
 }
 
@@ -564,8 +630,9 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
   // TMEM per slot: the accumulator (widest layer) then the A region (half the
   // widest hidden layer, two FP16 values per column), each a multiple of 32.
   const uint32_t acc_cols = (nmax + 31u) & ~31u;
-  const uint32_t a_cols = ((act_w / 2u) + 31u) & ~31u;
+  const uint32_t a_cols = ((act_w / 2u) + 8u + 31u) & ~31u;  // + the 8-column ones slab
   p.a_col = acc_cols;
+  p.a_ones = acc_cols + act_w / 2u;
   p.slot_cols = acc_cols + a_cols;
   // output staging: 8 KB per 32-column chunk, 4 KB for a trailing 16-column one
   p.out_slot_bytes = static_cast<uint32_t>(p.dL >> 5) * (kTileM * 64u) +
@@ -585,8 +652,10 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
         off += (variant == kVarRowMajor) ? 0u : align1024(p.bias_off);
         p.sm_sched = off;
         off += align1024(p.sched_bytes);
-        p.sm_bias = off;
-        off += align1024(nb * 4u);
+        p.sm_bslab = off;
+        off += align1024(p.bslab_bytes);
+        p.sm_ones = off;
+        off += kOnesTileBytes;
         p.sm_out = off;
         off += slots * obufs * p.out_slot_bytes;
         p.sm_b = off;

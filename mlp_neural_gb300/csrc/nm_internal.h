@@ -45,7 +45,7 @@ struct LayerInfo {
   int32_t K, N;
   uint32_t slab_begin, slab_end;  // range of this layer's k-slabs in the descriptor table
   uint32_t idesc;                 // tcgen05 instruction descriptor (M = 128, N)
-  uint32_t bias_f_off;            // float offset of b_l in the smem bias array
+  uint32_t bslab_off;             // byte offset of b_l's bias slab in the bias-slab region
   uint32_t rm_off;                // element offset of W_l in the row-major mirror
   uint32_t w_off;                 // byte offset of W_l's image in the blob / smem weight region
 };
@@ -67,9 +67,17 @@ static_assert(sizeof(LayerInfo) == 32, "layer table entry size");
 static_assert(sizeof(Schedule) % 16 == 0, "schedule must copy in 16-byte units");
 
 // Fills the schedule for a network and returns the number of bytes of it the
-// kernel copies to shared memory (layer table + the slabs in use).
+// kernel copies to shared memory (layer table + the slabs in use); *bslab_bytes
+// receives the size of the bias-slab region.
 uint32_t build_schedule(const int32_t* dims, int L, const uint32_t* w_off, const uint32_t* rm_off,
-                        Schedule& s);
+                        Schedule& s, uint32_t* bslab_bytes);
+
+// The bias enters through the tensor core: every layer's MMA chain ends with
+// one more K=16 MMA whose A slab is a "ones" column (A[r][0] = 1, the rest 0)
+// and whose B slab is the "bias slab" (B[n][0] = b[n], the rest 0), both in
+// the 32-byte-swizzle K-major layout. It adds b[n] to the FP32 accumulator
+// after the sum of products, as the arithmetic prescribes.
+constexpr uint32_t kOnesTileBytes = 128u * 32u;
 
 struct FusedParams {  // 128-byte aligned through its CUtensorMap members
   CUtensorMap tm_in[3];   // input [n][d0] maps, by swizzle kind (box 128 rows)
@@ -85,8 +93,11 @@ struct FusedParams {  // 128-byte aligned through its CUtensorMap members
   uint32_t bias_off;      // byte offset of the bias block in the blob (= weight image bytes)
   uint32_t n_bias;        // sum of d_1..d_L
   uint32_t sched_bytes;   // bytes of the schedule to copy
+  uint32_t bslab_bytes;   // bytes of the bias-slab region
+  uint32_t bias_row0[kMaxLayers];  // index of b_l[0] among the concatenated biases
+  uint32_t bslab_off[kMaxLayers];  // byte offset of b_l's slab in the bias-slab region
   // shared-memory plan (byte offsets from the 1024-aligned base)
-  uint32_t sm_w, sm_sched, sm_bias, sm_in, sm_out, sm_b, sm_bar;
+  uint32_t sm_w, sm_sched, sm_bslab, sm_ones, sm_in, sm_out, sm_b, sm_bar;
   uint32_t in_stage_bytes, out_slot_bytes, b_stage_bytes;
   uint32_t n_in_stages;  // input stages per slot
   uint32_t n_b_stages, n_out_bufs;
@@ -94,6 +105,7 @@ struct FusedParams {  // 128-byte aligned through its CUtensorMap members
   uint32_t tmem_cols;   // allocated TMEM columns (power of two)
   uint32_t slot_cols;   // TMEM columns per tile slot: accumulator, then the A region
   uint32_t a_col;       // column of the A region (next layer's FP16 activations) in a slot
+  uint32_t a_ones;      // column of the constant "ones" A slab (8 columns) in a slot
   uint64_t wait_ns;     // limit of every pipeline wait
   uint32_t test_stall;  // non-zero: the MMA thread first waits on kBarNever
 };
