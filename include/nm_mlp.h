@@ -160,6 +160,34 @@ nm_status nm_mlp_set_wait_limit(nm_mlp *h, uint64_t nanoseconds);
  * any fault. The outputs of such a launch are undefined. */
 nm_status nm_mlp_set_test_stall(nm_mlp *h, int32_t enable);
 
+/* Inference that allocates no device memory. The source pages have no
+ * counterpart to this call; it exists for callers that cannot call
+ * cudaMalloc -- code embedded in a host application that owns the device's
+ * whole memory budget, or a latency-critical path where an allocation's
+ * implicit synchronisation is not allowed -- but that can pass device buffers
+ * they already own.
+ * W, b: host arrays of L device pointers to the row-major FP16 weights
+ *       [dims[l+1]][dims[l]] and biases [dims[l+1]] (as for pack_weights);
+ * in, out, n, stream: as for nm_mlp_infer.
+ * Every call packs the weights again and runs the fused kernel (fused
+ * variant) out of one library-owned, file-scope device array of 1 MiB, which
+ * every GPU that loads the library holds until the process exits. Networks
+ * whose packed weights and biases exceed 1,043,456 bytes are rejected with
+ * NM_ERR_UNSUPPORTED (the page-shaped network needs 58,272; the widest
+ * 256-wide 16-layer network would need about 2 MB).
+ * The first call on a device looks up that array's device address with the
+ * device current (a one-time set-up); make that first call before any stream
+ * capture. All calls share the array and it keeps the last call's contents
+ * (each call clears what must start at zero): calls whose work overlaps on the
+ * GPU -- from several host threads, or on several streams -- race and must
+ * not be made.
+ * The call returns after `stream` has completed the work (it synchronises the
+ * stream), so a kernel-side give-up is reported directly as NM_ERR_TIMEOUT.
+ * Errors: NM_ERR_INVALID_ARG, NM_ERR_UNSUPPORTED, NM_ERR_CUDA, NM_ERR_TIMEOUT. */
+nm_status nm_mlp_infer_noalloc(const int32_t *dims, int32_t n_dims, const void *const *W,
+                               const void *const *b, const void *in, int64_t n, void *out,
+                               nm_stream stream);
+
 /* Free the handle and its device memory (synchronises the device first).
  * NULL is a no-op. */
 void nm_mlp_destroy(nm_mlp *h);

@@ -41,6 +41,7 @@ SIGNATURES = {
     "nm_mlp_device_status": (ctypes.c_int, [_P, _P]),
     "nm_mlp_set_wait_limit": (ctypes.c_int, [_P, ctypes.c_uint64]),
     "nm_mlp_set_test_stall": (ctypes.c_int, [_P, ctypes.c_int32]),
+    "nm_mlp_infer_noalloc": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, _P, ctypes.c_int64, _P, _P]),
     "nm_mlp_destroy": (None, [_P]),
 }
 
@@ -97,6 +98,17 @@ def _stream(stream) -> int:
     if isinstance(stream, int):
         return stream
     return int(stream.cuda_stream)
+
+
+def infer_noalloc(dims, W, b, x, out, stream=None) -> int:
+    """nm_mlp_infer_noalloc: inference without any device allocation by the
+    library (for callers that cannot allocate); returns the status code."""
+    d = (ctypes.c_int32 * len(dims))(*[int(v) for v in dims])
+    Wp = (ctypes.c_void_p * len(W))(*[_addr(w) for w in W])
+    bp = (ctypes.c_void_p * len(b))(*[_addr(v) for v in b])
+    n = x.shape[0] if hasattr(x, "shape") else 0
+    return lib().nm_mlp_infer_noalloc(d, len(dims), Wp, bp, _addr(x), int(n), _addr(out),
+                                      _stream(stream))
 
 
 class MLP:
