@@ -1,0 +1,78 @@
+"""The C-ABI library loads on a machine without a GPU and exports every symbol
+include/nm_mlp.h declares; host-side argument checks answer without touching
+a device. (CPU only: no compute call is made.)"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nm_mlp.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nm_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def nmlib():
+    from mlp_neural_gb300 import build, nm
+    build.build()
+    return nm
+
+
+def test_header_declares_the_problem_statement_calls():
+    names = _declared_functions()
+    for required in ("nm_mlp_create", "nm_mlp_pack_weights", "nm_mlp_infer", "nm_mlp_destroy",
+                     "nm_mlp_packed_size"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(nmlib):
+    L = ctypes.CDLL(nmlib.LIB_PATH)
+    missing = [n for n in _declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+    # the binding covers exactly the declared calls
+    assert sorted(nmlib.SIGNATURES) == _declared_functions()
+
+
+def test_status_strings(nmlib):
+    for code in range(7):
+        assert nmlib.status_str(code).startswith("NM_")
+    assert nmlib.status_str(nmlib.NM_ERR_TIMEOUT) == "NM_ERR_TIMEOUT"
+    assert nmlib.lib().nm_abi_version() >= 1
+
+
+@pytest.mark.parametrize("dims,expect", [
+    ((32,), 1),                 # fewer than two widths
+    ((32, 24), 2),              # not a multiple of 16
+    ((32, 272), 2),             # wider than 256
+    ((16,) * 18, 2),            # more than 16 layers
+])
+def test_create_rejects_bad_dims_on_the_host(nmlib, dims, expect):
+    h = ctypes.c_void_p()
+    arr = (ctypes.c_int32 * len(dims))(*dims)
+    assert nmlib.lib().nm_mlp_create(arr, len(dims), ctypes.byref(h)) == expect
+    assert h.value is None
+
+
+def test_null_handles_are_invalid(nmlib):
+    L = nmlib.lib()
+    assert L.nm_mlp_infer(None, None, 0, None, None) == nmlib.NM_ERR_INVALID_ARG
+    assert L.nm_mlp_set_variant(None, 0) == nmlib.NM_ERR_INVALID_ARG
+    assert L.nm_mlp_device_status(None, None) == nmlib.NM_ERR_INVALID_ARG
+    n = ctypes.c_size_t()
+    assert L.nm_mlp_packed_size(None, ctypes.byref(n)) == nmlib.NM_ERR_INVALID_ARG
+    L.nm_mlp_destroy(None)  # no-op
+
+
+def test_noalloc_argument_checks_on_the_host(nmlib):
+    L = nmlib.lib()
+    dims = (ctypes.c_int32 * 2)(32, 24)
+    null2 = (ctypes.c_void_p * 1)(None)
+    assert L.nm_mlp_infer_noalloc(dims, 2, null2, null2, None, 4, None, None) == nmlib.NM_ERR_UNSUPPORTED
+    dims = (ctypes.c_int32 * 2)(32, 16)
+    assert L.nm_mlp_infer_noalloc(dims, 2, null2, null2, None, 4, None, None) == nmlib.NM_ERR_INVALID_ARG
