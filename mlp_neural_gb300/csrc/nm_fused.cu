@@ -73,6 +73,10 @@ struct Ctx {
   }
 };
 
+__host__ __device__ constexpr bool is_scalar_act(int V) {
+  return V == kVarScalar || V == kVarScalarStream;
+}
+
 // LayerInfo as loaded from shared memory (two 16-byte loads).
 struct LayerRegs {
   int32_t K, N;
@@ -171,13 +175,13 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t* acc, int npairs, 
   for (int j = 0; j < 16; ++j) {
     if (j < npairs) {
       __half2 h = __floats2half2_rn(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
-      if (V != kVarScalar) {
+      if (!is_scalar_act(V)) {
         if (act) h = __hmax2(h, __hmul2(h, slope2));
       }
       out[j] = *reinterpret_cast<uint32_t*>(&h);
     }
   }
-  if (V == kVarScalar && act) {
+  if (is_scalar_act(V) && act) {
     // The page's indexed-lane form: every FP16 value visited one by one with
     // a dynamic index and a branch.
     __half lanes[32];
@@ -353,6 +357,141 @@ __device__ __forceinline__ void run_slot_control(const FusedParams& p, const Ctx
   }
 }
 
+// ------------------------------------------------------------------ streamed weights
+// Networks whose packed weights do not fit next to the pipeline buffers
+// stream them: a producer thread (an otherwise idle control warp) copies each
+// layer's K-segments -- each a contiguous N x 2w-byte piece of the packed
+// image, at most 32 KB -- into a shared ring, in the order (round, layer,
+// segment) in which every slot's control thread consumes them. A stage is
+// released once every slot's MMAs on it have completed (or, for a slot with
+// no tile in that round, once it has seen the stage).
+
+__device__ __forceinline__ bool is_stream(int V) { return V == kVarFusedStream || V == kVarScalarStream; }
+
+__device__ __forceinline__ void run_weight_producer(const FusedParams& p, const Ctx& c) {
+  const int32_t S = static_cast<int32_t>(p.n_slots);
+  const int32_t n_rounds = (c.n_local + S - 1) / S;
+  const uint32_t RW = p.n_wstages;
+  bool ok = wait_phase(c.bar(kBarWLoad), 0, p.wait_ns, c.abort_flag, p.status);
+  uint32_t g = 0;
+  for (int32_t r = 0; r < n_rounds && ok; ++r) {
+    for (int l = 0; l < p.L && ok; ++l) {
+      const LayerRegs li = load_layer(p, c, l);
+      for (int k = 0; k < li.K && ok;) {
+        uint32_t off;
+        int w, k0;
+        locate(static_cast<uint32_t>(li.N), li.K, k, off, w, k0);
+        const uint32_t st = g % RW;
+        ok = wait_phase(c.bar(kBarWEmpty + st), ((g / RW) & 1u) ^ 1u, p.wait_ns, c.abort_flag,
+                        p.status);
+        if (!ok) break;
+        const uint32_t bytes = static_cast<uint32_t>(li.N) * 2u * static_cast<uint32_t>(w);
+        mbar_arrive_expect_tx(c.bar(kBarWFull + st), bytes);
+        bulk_load(c.sbase + p.sm_wring + st * p.wstage_bytes, p.blob + li.w_off + off, bytes,
+                  c.bar(kBarWFull + st));
+        ++g;
+        k = k0 + w;
+      }
+    }
+  }
+  // Drain: the last copies issued must land before the CTA may exit.
+  const uint32_t first = g > RW ? g - RW : 0u;
+  for (uint32_t gg = first; gg < g; ++gg)
+    wait_drain(c.bar(kBarWFull + gg % RW), (gg / RW) & 1u, p.status);
+}
+
+template <int V>
+__device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, const Ctx& c,
+                                                        int32_t s) {
+  const int32_t S = static_cast<int32_t>(p.n_slots);
+  const uint32_t D = p.n_in_stages;
+  const uint32_t RW = p.n_wstages;
+  const int L = p.L;
+  const int32_t n_rounds_all = (c.n_local + S - 1) / S;   // rounds of the whole CTA
+  const int32_t n_rounds = (c.n_local - s + S - 1) / S;   // rounds with a tile of this slot
+  int32_t issued = -1;
+  bool ok = true;
+  if (p.test_stall) ok = wait_phase(c.bar(kBarNever), 0, p.wait_ns, c.abort_flag, p.status);
+  if (ok) ok = wait_phase(c.bar(kBarWLoad), 0, p.wait_ns, c.abort_flag, p.status);
+  const uint32_t slot_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
+  uint32_t g = 0;  // weight stages consumed
+  for (int32_t r = 0; r < n_rounds_all && ok; ++r) {
+    const bool has_tile = r < n_rounds;
+    while (ok && has_tile && issued + 1 < r + static_cast<int32_t>(D) && issued + 1 < n_rounds) {
+      const uint32_t rr = static_cast<uint32_t>(issued + 1);
+      const uint32_t st = static_cast<uint32_t>(s) * D + rr % D;
+      ok = wait_phase(c.bar(kBarInEmpty + st), ((rr / D) & 1u) ^ 1u, p.wait_ns, c.abort_flag,
+                      p.status);
+      if (!ok) break;
+      mbar_arrive_expect_tx(c.bar(kBarInFull + st), static_cast<uint32_t>(kTileM * 2 * p.d0));
+      issue_input_tma(p, c.sbase + p.sm_in + st * p.in_stage_bytes, c.bar(kBarInFull + st),
+                      tile_of(static_cast<int32_t>(rr) * S + s));
+      issued = static_cast<int32_t>(rr);
+    }
+    const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(r) % D;
+    for (int l = 0; l < L && ok; ++l) {
+      const LayerRegs li = load_layer(p, c, l);
+      if (has_tile) {
+        const int32_t q = r * L + l - 1;
+        if (q >= 0)
+          ok = spin_phase(c.bar(kBarActReady + s), static_cast<uint32_t>(q) & 1u, p.wait_ns,
+                          c.abort_flag, p.status);
+        if (ok && l == 0)
+          ok = wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(r) / D) & 1u, p.wait_ns,
+                          c.abort_flag, p.status);
+      }
+      const uint32_t in_base = c.sbase + p.sm_in + st * p.in_stage_bytes;
+      for (int k = 0; k < li.K && ok;) {
+        uint32_t boff, aoff;
+        int w, k0;
+        locate(static_cast<uint32_t>(li.N), li.K, k, boff, w, k0);
+        locate(kTileM, li.K, k, aoff, w, k0);
+        const uint32_t ws = g % RW;
+        ok = wait_phase(c.bar(kBarWFull + ws), (g / RW) & 1u, p.wait_ns, c.abort_flag, p.status);
+        if (!ok) break;
+        if (has_tile) {
+          tc_fence_after_sync();
+          const uint32_t stage = c.sbase + p.sm_wring + ws * p.wstage_bytes;
+          const uint32_t sbo = 16u * static_cast<uint32_t>(w);
+          for (int kk = k0; kk < k0 + w; kk += 16) {
+            const uint32_t kb = static_cast<uint32_t>(kk - k0) * 2u;
+            const uint64_t bd = smem_desc(stage + kb, sbo, swizzle_code(w));
+            const uint32_t acc = kk > 0 ? 1u : 0u;
+            if (l == 0)
+              umma_f16_ss(slot_tmem, smem_desc(in_base + aoff + kb, sbo, swizzle_code(w)), bd,
+                          li.idesc, acc);
+            else
+              umma_f16_ts(slot_tmem, slot_tmem + p.a_col + static_cast<uint32_t>(kk >> 1), bd,
+                          li.idesc, acc);
+          }
+          umma_commit(c.bar(kBarWEmpty + ws));
+        } else {
+          mbar_arrive(c.bar(kBarWEmpty + ws));
+        }
+        ++g;
+        k = k0 + w;
+      }
+      if (ok && has_tile) {
+        // Bias: one more K=16 MMA, ones column x bias slab, added last.
+        const uint64_t bias_bd = smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u);
+        if (l == 0)
+          umma_f16_ss(slot_tmem, smem_desc(c.sbase + p.sm_ones, 256u, 6u), bias_bd, li.idesc, 1u);
+        else
+          umma_f16_ts(slot_tmem, slot_tmem + p.a_ones, bias_bd, li.idesc, 1u);
+        umma_commit(c.bar(kBarAccFull + s));
+        if (l == 0) umma_commit(c.bar(kBarInEmpty + st));
+      }
+    }
+  }
+  umma_commit(c.bar(kBarDrain + s));
+  wait_drain(c.bar(kBarDrain + s), 0, p.status);
+  const int32_t lo = issued - static_cast<int32_t>(D) + 1 > 0 ? issued - static_cast<int32_t>(D) + 1 : 0;
+  for (int32_t rr = lo; rr <= issued; ++rr) {
+    const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(rr) % D;
+    wait_drain(c.bar(kBarInFull + st), (static_cast<uint32_t>(rr) / D) & 1u, p.status);
+  }
+}
+
 // ------------------------------------------------------------------ epilogue
 // Output staging of one tile: a region per 32-column chunk of the output
 // (128 rows x 64 bytes, 64-byte swizzle; a trailing 16-column chunk gets
@@ -512,6 +651,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       mbar_init(c.bar(kBarDrain + s), 1);
     }
     for (int s = 0; s < kMaxBStages; ++s) mbar_init(c.bar(kBarBEmpty + s), 1);
+    for (int s = 0; s < kMaxWStages; ++s) {
+      mbar_init(c.bar(kBarWFull + s), 1);
+      mbar_init(c.bar(kBarWEmpty + s), p.n_slots);
+    }
     mbar_init(c.bar(kBarWLoad), 1);
     mbar_init(c.bar(kBarNever), 1);
     *c.abort_flag = 0u;
@@ -555,7 +698,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   if (warp == 0 && lane == 0) {
     // Stage the schedule (and the packed weight images) once for the whole
     // persistent loop.
-    const uint32_t wbytes = (V == kVarRowMajor) ? 0u : p.bias_off;
+    const uint32_t wbytes = (V == kVarRowMajor || is_stream(V)) ? 0u : p.bias_off;
     mbar_arrive_expect_tx(c.bar(kBarWLoad), p.sched_bytes + wbytes);
     bulk_load(c.sbase + p.sm_sched, p.sched, p.sched_bytes, c.bar(kBarWLoad));
     for (uint32_t off = 0; off < wbytes; off += 32768u) {
@@ -564,7 +707,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
   }
   if (warp < kCtrlWarps) {
-    if (warp < static_cast<int>(p.n_slots)) run_slot_control<V>(p, c, warp, lane);
+    if (is_stream(V)) {
+      if (lane == 0) {
+        if (warp < static_cast<int>(p.n_slots))
+          run_slot_control_stream<V>(p, c, warp);
+        else if (warp == static_cast<int>(p.n_slots))
+          run_weight_producer(p, c);
+      }
+      __syncwarp();
+    } else if (warp < static_cast<int>(p.n_slots)) {
+      run_slot_control<V>(p, c, warp, lane);
+    }
     if (warp == 0 && lane == 0) wait_drain(c.bar(kBarWLoad), 0, p.status);
   } else {
     run_epilogue<V>(p, c, warp, lane);
@@ -639,42 +792,66 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
                      ((p.dL & 31) ? kTileM * 32u : 0u);
   p.b_stage_bytes = (variant == kVarRowMajor) ? align1024(bstage) : 0u;
   const uint32_t stage = align1024(image_bytes(kTileM, p.d0));
+  // Streamed weights: a ring of stages, each one K-segment of one layer.
+  uint32_t wseg = 0;
+  for (int l = 0; l < L; ++l) {
+    const uint32_t wmax = dims[l] >= 64 ? 64u : (dims[l] >= 32 ? 32u : 16u);
+    const uint32_t b = static_cast<uint32_t>(dims[l + 1]) * 2u * wmax;
+    wseg = b > wseg ? b : wseg;
+  }
+  wseg = align1024(wseg);
 
-  // Most tile slots first (4, 2, 1) as TMEM allows, then two input stages
-  // per slot before one, then two output buffers per slot before one.
-  for (uint32_t slots = kMaxSlots; slots >= 1; slots >>= 1) {
-    if (slots * p.slot_cols > 512u) continue;
-    p.n_b_stages = (variant == kVarRowMajor) ? 2u * slots : 0u;
-    for (uint32_t depth = 2; depth >= 1; --depth) {
-      for (uint32_t obufs = kOutBufs; obufs >= 1; --obufs) {
-        uint32_t off = 0;
-        p.sm_w = 0;
-        off += (variant == kVarRowMajor) ? 0u : align1024(p.bias_off);
-        p.sm_sched = off;
-        off += align1024(p.sched_bytes);
-        p.sm_bslab = off;
-        off += align1024(p.bslab_bytes);
-        p.sm_ones = off;
-        off += kOnesTileBytes;
-        p.sm_out = off;
-        off += slots * obufs * p.out_slot_bytes;
-        p.sm_b = off;
-        off += p.n_b_stages * p.b_stage_bytes;
-        p.sm_bar = off;
-        off += 1024u;  // barrier block, keeps the input ring 1024-aligned
-        p.sm_in = off;
-        off += slots * depth * stage;
-        const uint32_t total = off + 1024u;  // + alignment slack of the dynamic smem base
-        if (total <= smem_optin) {
-          uint32_t cols = 32;
-          while (cols < slots * p.slot_cols) cols <<= 1;
-          p.tmem_cols = cols;
-          p.n_slots = slots;
-          p.in_stage_bytes = stage;
-          p.n_in_stages = depth;
-          p.n_out_bufs = obufs;
-          return total;
+  // Resident weights first (most tile slots, 4, 2, 1, as TMEM allows; two
+  // input stages per slot before one; two output buffers before one). If the
+  // weights do not fit (fused and scalar-activation variants), stream them
+  // with at most 2 slots (a control warp must stay free to produce) and the
+  // deepest weight ring (4 down to 2 stages) that fits.
+  for (int mode = 0; mode < 2; ++mode) {
+    const bool streamed = mode == 1;
+    if (streamed && variant == kVarRowMajor) break;
+    for (uint32_t slots = kMaxSlots; slots >= 1; slots >>= 1) {
+      if (slots * p.slot_cols > 512u) continue;
+      if (streamed && slots > 2) continue;
+      p.n_b_stages = (variant == kVarRowMajor) ? 2u * slots : 0u;
+      for (uint32_t wst = streamed ? kMaxWStages : 0u; wst >= (streamed ? 2u : 0u); --wst) {
+        for (uint32_t depth = 2; depth >= 1; --depth) {
+          for (uint32_t obufs = kOutBufs; obufs >= 1; --obufs) {
+            uint32_t off = 0;
+            p.sm_w = 0;
+            off += (variant == kVarRowMajor || streamed) ? 0u : align1024(p.bias_off);
+            p.sm_sched = off;
+            off += align1024(p.sched_bytes);
+            p.sm_bslab = off;
+            off += align1024(p.bslab_bytes);
+            p.sm_ones = off;
+            off += kOnesTileBytes;
+            p.sm_out = off;
+            off += slots * obufs * p.out_slot_bytes;
+            p.sm_b = off;
+            off += p.n_b_stages * p.b_stage_bytes;
+            p.sm_wring = off;
+            off += wst * wseg;
+            p.sm_bar = off;
+            off += 1024u;  // barrier block, keeps the input ring 1024-aligned
+            p.sm_in = off;
+            off += slots * depth * stage;
+            const uint32_t total = off + 1024u;  // + alignment slack of the dynamic smem base
+            if (total <= smem_optin) {
+              uint32_t cols = 32;
+              while (cols < slots * p.slot_cols) cols <<= 1;
+              p.tmem_cols = cols;
+              p.n_slots = slots;
+              p.in_stage_bytes = stage;
+              p.n_in_stages = depth;
+              p.n_out_bufs = obufs;
+              p.stream_w = streamed ? 1u : 0u;
+              p.n_wstages = wst;
+              p.wstage_bytes = wseg;
+              return total;
+            }
+          }
         }
+        if (!streamed) break;
       }
     }
   }
@@ -699,6 +876,11 @@ static cudaError_t launch_variant(const FusedParams& p, int grid, uint32_t smem,
 
 cudaError_t launch_fused(const FusedParams& p, int variant, int grid, uint32_t smem,
                          cudaStream_t stream) {
+  if (p.stream_w) {
+    if (variant == kVarFused) return launch_variant<kVarFusedStream>(p, grid, smem, stream);
+    if (variant == kVarScalar) return launch_variant<kVarScalarStream>(p, grid, smem, stream);
+    return cudaErrorInvalidValue;
+  }
   switch (variant) {
     case kVarFused: return launch_variant<kVarFused>(p, grid, smem, stream);
     case kVarRowMajor: return launch_variant<kVarRowMajor>(p, grid, smem, stream);

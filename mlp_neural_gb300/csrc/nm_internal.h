@@ -21,7 +21,17 @@ constexpr int kOutBufs = 2;        // output staging buffers per slot (TMA-store
 constexpr int kMaxSlabs = kMaxLayers * (kMaxDim / 16);
 constexpr uint32_t kStatusTimeout = 1u;
 
-enum Variant : int { kVarFused = 0, kVarRowMajor = 1, kVarScalar = 2 };
+// Public variants 0..2 (nm_variant); 3 and 4 are the fused and the
+// scalar-activation kernels with streamed instead of resident weights, chosen
+// by the planner when the packed weights do not fit in shared memory.
+enum Variant : int {
+  kVarFused = 0,
+  kVarRowMajor = 1,
+  kVarScalar = 2,
+  kVarFusedStream = 3,
+  kVarScalarStream = 4
+};
+constexpr int kMaxWStages = 4;     // streamed-weight ring depth (upper bound)
 
 // Barrier slots inside the barrier block of the fused kernel's smem. Input
 // stage s * n_in_stages + k belongs to slot s; likewise B stages 2s, 2s + 1.
@@ -31,7 +41,9 @@ enum BarIndex : int {
   kBarAccFull = kBarInEmpty + kMaxInStages,
   kBarActReady = kBarAccFull + kMaxSlots,
   kBarBEmpty = kBarActReady + kMaxSlots,
-  kBarWLoad = kBarBEmpty + kMaxBStages,
+  kBarWFull = kBarBEmpty + kMaxBStages,   // streamed-weight ring
+  kBarWEmpty = kBarWFull + 4,
+  kBarWLoad = kBarWEmpty + 4,
   kBarDrain = kBarWLoad + 1,  // one per slot
   kBarNever = kBarDrain + kMaxSlots,  // never signalled (failure-path test hook)
   kBarCount = kBarNever + 1
@@ -97,7 +109,7 @@ struct FusedParams {  // 128-byte aligned through its CUtensorMap members
   uint32_t bias_row0[kMaxLayers];  // index of b_l[0] among the concatenated biases
   uint32_t bslab_off[kMaxLayers];  // byte offset of b_l's slab in the bias-slab region
   // shared-memory plan (byte offsets from the 1024-aligned base)
-  uint32_t sm_w, sm_sched, sm_bslab, sm_ones, sm_in, sm_out, sm_b, sm_bar;
+  uint32_t sm_w, sm_sched, sm_bslab, sm_ones, sm_in, sm_out, sm_b, sm_wring, sm_bar;
   uint32_t in_stage_bytes, out_slot_bytes, b_stage_bytes;
   uint32_t n_in_stages;  // input stages per slot
   uint32_t n_b_stages, n_out_bufs;
@@ -106,6 +118,9 @@ struct FusedParams {  // 128-byte aligned through its CUtensorMap members
   uint32_t slot_cols;   // TMEM columns per tile slot: accumulator, then the A region
   uint32_t a_col;       // column of the A region (next layer's FP16 activations) in a slot
   uint32_t a_ones;      // column of the constant "ones" A slab (8 columns) in a slot
+  uint32_t stream_w;    // 1: weights streamed through the ring instead of resident
+  uint32_t n_wstages;   // streamed-weight ring depth
+  uint32_t wstage_bytes;
   uint64_t wait_ns;     // limit of every pipeline wait
   uint32_t test_stall;  // non-zero: the MMA thread first waits on kBarNever
 };

@@ -21,6 +21,9 @@ SMALL_DIMS = [
     (64, 128, 128, 32),
     (32, 48, 96, 208, 16),
 ]
+# Networks whose packed weights do not fit in shared memory: the kernel
+# streams their weights (wide: 2 tile slots, heterogeneous: 1).
+STREAMED_DIMS = [synth.WORKLOADS["wide"].dims, synth.WORKLOADS["hetero"].dims]
 SENTINEL = 0x7E7E  # a NaN pattern the kernel never produces from finite data
 
 
@@ -60,7 +63,7 @@ def test_pack_bit_exact(orc, dims):
         assert np.array_equal(to_host(W2[l]), W[l]) and np.array_equal(to_host(b2[l]), b[l])
 
 
-@pytest.mark.parametrize("dims", SMALL_DIMS)
+@pytest.mark.parametrize("dims", SMALL_DIMS + STREAMED_DIMS)
 @pytest.mark.parametrize("n", [1, 127, 128, 129, 255, 4097])
 def test_infer_matches_oracle(orc, dims, n):
     W, b, x = synth.small_net_inputs(dims, seed=n + dims[0], n=n)
@@ -92,7 +95,7 @@ def _dyadic_net(dims, seed, n):
     return W, b, x
 
 
-@pytest.mark.parametrize("dims", SMALL_DIMS)
+@pytest.mark.parametrize("dims", SMALL_DIMS + STREAMED_DIMS)
 def test_dyadic_networks_bit_exact(orc, dims):
     W, b, x = _dyadic_net(dims, seed=len(dims) * 7 + dims[-2], n=1000)
     m = make_net(dims, W, b)
@@ -139,6 +142,13 @@ def test_ablation_variants_bit_identical(dims):
     y1 = _run(m, x, variant=1)
     y2 = _run(m, x, variant=2)
     assert np.array_equal(y0, y1) and np.array_equal(y0, y2)
+
+
+@pytest.mark.parametrize("dims", STREAMED_DIMS)
+def test_streamed_weights_scalar_activation_bit_identical(dims):
+    W, b, x = synth.small_net_inputs(dims, seed=8, n=3000)
+    m = make_net(dims, W, b)
+    assert np.array_equal(_run(m, x, variant=0), _run(m, x, variant=2))
 
 
 def test_empty_batch_and_argument_errors():
@@ -221,3 +231,33 @@ def test_full_page(orc):
 
 def test_full_ablation_all_variants(orc):
     _full_workload(orc, "ablation", variants=(0, 1, 2))
+
+
+def _full_sampled(orc, name, n_samples=4096):
+    """The full workload in one dispatch; the oracle checks a sample of rows:
+    the first and last tiles plus random rows."""
+    import torch
+    w = synth.WORKLOADS[name]
+    W, b = synth.net_params(w.dims, w.seed)
+    x = synth.inputs(w)
+    m = make_net(w.dims, W, b)
+    xd = to_dev(x)
+    out = torch.empty((w.n_evals, w.dims[-1]), dtype=torch.float16, device="cuda")
+    m.infer(xd, out)
+    torch.cuda.synchronize()
+    assert m.device_status() == nm().NM_OK
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([np.arange(256), np.arange(w.n_evals - 256, w.n_evals),
+                                     rng.integers(0, w.n_evals, n_samples)]))
+    idx = torch.from_numpy(rows).cuda()
+    y = to_host(out.index_select(0, idx))
+    assert_close(y, orc.forward(w.dims, W, b, x[rows]), name)
+    assert not np.isnan(to_host(out).view(np.float16)).any()
+
+
+def test_full_wide_sampled(orc):
+    _full_sampled(orc, "wide")
+
+
+def test_full_hetero_sampled(orc):
+    _full_sampled(orc, "hetero")
