@@ -85,7 +85,7 @@ struct LayerRegs {
 
 __device__ __forceinline__ LayerRegs load_layer(const FusedParams& p, const Ctx& c, int l) {
   const uint32_t a = c.layer_addr(p, l);
-  const uint4 x = ld_shared_u32x4(a), y = ld_shared_u32x4(a + 16);
+  const uint4 x = ld_shared_const_u32x4(a), y = ld_shared_const_u32x4(a + 16);
   LayerRegs r;
   r.K = static_cast<int32_t>(x.x);
   r.N = static_cast<int32_t>(x.y);
@@ -166,27 +166,22 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const F
 }
 
 // FP32 accumulator pairs (bias already added by the tensor core) -> FP16
-// pairs (round to nearest even), then the activation when `act` is set.
-// Column 2j goes to the low half.
-template <int V>
-__device__ __forceinline__ void epilogue_chunk(const uint32_t* acc, int npairs, bool act,
-                                               __half2 slope2, uint32_t* out) {
+// pairs (round to nearest even), then, for hidden layers (ACT), the
+// activation. Column 2j goes to the low half. NP pairs, unrolled.
+template <int V, int NP, bool ACT>
+__device__ __forceinline__ void convert_pairs(const uint32_t* acc, __half2 slope2, uint32_t* out) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    if (j < npairs) {
-      __half2 h = __floats2half2_rn(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
-      if (!is_scalar_act(V)) {
-        if (act) h = __hmax2(h, __hmul2(h, slope2));
-      }
-      out[j] = *reinterpret_cast<uint32_t*>(&h);
-    }
+  for (int j = 0; j < NP; ++j) {
+    __half2 h = __floats2half2_rn(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
+    if (ACT && !is_scalar_act(V)) h = __hmax2(h, __hmul2(h, slope2));
+    out[j] = *reinterpret_cast<uint32_t*>(&h);
   }
-  if (is_scalar_act(V) && act) {
+  if (ACT && is_scalar_act(V)) {
     // The page's indexed-lane form: every FP16 value visited one by one with
     // a dynamic index and a branch.
-    __half lanes[32];
+    __half lanes[2 * NP];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < NP; ++j) {
       __half2 h = *reinterpret_cast<__half2*>(&out[j]);
       lanes[2 * j] = __low2half(h);
       lanes[2 * j + 1] = __high2half(h);
@@ -194,11 +189,11 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t* acc, int npairs, 
     const __half slope = __low2half(slope2);
     const __half zero = __float2half_rn(0.0f);
 #pragma unroll 1
-    for (int e = 0; e < 2 * npairs; ++e) {
+    for (int e = 0; e < 2 * NP; ++e) {
       if (__hlt(lanes[e], zero)) lanes[e] = __hmul(lanes[e], slope);
     }
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < NP; ++j) {
       __half2 h = __halves2half2(lanes[2 * j], lanes[2 * j + 1]);
       out[j] = *reinterpret_cast<uint32_t*>(&h);
     }
@@ -287,11 +282,6 @@ __device__ __forceinline__ void run_slot_control(const FusedParams& p, const Ctx
         __syncwarp();
       }
       if (lane == 0) {
-        // Descriptors of the first k-slabs, fetched before the wait.
-        uint4 pre[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if (li.slab_begin + k < li.slab_end) pre[k] = ld_shared_u32x4(c.slab_addr(p, li.slab_begin + k));
         const int32_t q = r * L + l - 1;  // completion of this slot's previous epilogue
         if (q >= 0)
           ok = spin_phase(c.bar(kBarActReady + s), static_cast<uint32_t>(q) & 1u, p.wait_ns,
@@ -301,40 +291,34 @@ __device__ __forceinline__ void run_slot_control(const FusedParams& p, const Ctx
                           c.abort_flag, p.status);
         if (ok) {
           tc_fence_after_sync();
+          // The MMA sequences below are straight-line loops: a branch between
+          // two tcgen05.mma instructions roughly doubles their issue cost.
           const uint64_t b_add = b_base >> 4;
           const uint32_t slot_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
-          // Layer 1 reads A (the input tile) from shared memory; later layers
-          // read the previous epilogue's FP16 output from TMEM, 8 columns per
-          // 16-wide k-slab.
-          const uint64_t a_add =
-              (l == 0) ? static_cast<uint64_t>((c.sbase + p.sm_in + st * p.in_stage_bytes) >> 4) : 0ull;
-          const uint32_t a_tmem = slot_tmem + p.a_col;
           const uint32_t nslab = li.slab_end - li.slab_begin;
-#pragma unroll
-          for (uint32_t k = 0; k < 4; ++k) {
-            if (k < nslab) {
-              const uint64_t bd = (static_cast<uint64_t>(pre[k].w) << 32 | pre[k].z) + b_add;
-              if (l == 0)
-                umma_f16_ss(slot_tmem, (static_cast<uint64_t>(pre[k].y) << 32 | pre[k].x) + a_add, bd,
-                            li.idesc, k > 0 ? 1u : 0u);
-              else
-                umma_f16_ts(slot_tmem, a_tmem + 8u * k, bd, li.idesc, k > 0 ? 1u : 0u);
-            }
-          }
-          for (uint32_t k = 4; k < nslab; ++k) {
-            const uint4 sd = ld_shared_u32x4(c.slab_addr(p, li.slab_begin + k));
-            const uint64_t bd = (static_cast<uint64_t>(sd.w) << 32 | sd.z) + b_add;
-            if (l == 0)
-              umma_f16_ss(slot_tmem, (static_cast<uint64_t>(sd.y) << 32 | sd.x) + a_add, bd, li.idesc, 1u);
-            else
-              umma_f16_ts(slot_tmem, a_tmem + 8u * k, bd, li.idesc, 1u);
-          }
-          // Bias: one more K=16 MMA, ones column x bias slab, added last.
+          const uint32_t tab = c.slab_addr(p, li.slab_begin);
           const uint64_t bias_bd = smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u);
-          if (l == 0)
+          if (l == 0) {
+            // Layer 1: A is the input tile in shared memory.
+            const uint64_t a_add = (c.sbase + p.sm_in + st * p.in_stage_bytes) >> 4;
+            for (uint32_t k = 0; k < nslab; ++k) {
+              const uint4 sd = ld_shared_const_u32x4(tab + 16u * k);
+              umma_f16_ss(slot_tmem, (static_cast<uint64_t>(sd.y) << 32 | sd.x) + a_add,
+                          (static_cast<uint64_t>(sd.w) << 32 | sd.z) + b_add, li.idesc, k);
+            }
+            // Bias: one more K=16 MMA, ones column x bias slab, added last.
             umma_f16_ss(slot_tmem, smem_desc(c.sbase + p.sm_ones, 256u, 6u), bias_bd, li.idesc, 1u);
-          else
+          } else {
+            // Later layers: A is the previous epilogue's FP16 output in TMEM,
+            // 8 columns per 16-wide k-slab.
+            const uint32_t a_tmem = slot_tmem + p.a_col;
+            for (uint32_t k = 0; k < nslab; ++k) {
+              const uint4 sd = ld_shared_const_u32x4(tab + 16u * k);
+              umma_f16_ts(slot_tmem, a_tmem + 8u * k,
+                          (static_cast<uint64_t>(sd.w) << 32 | sd.z) + b_add, li.idesc, k);
+            }
             umma_f16_ts(slot_tmem, slot_tmem + p.a_ones, bias_bd, li.idesc, 1u);
+          }
           umma_commit(c.bar(kBarAccFull + s));
           if (l == 0) umma_commit(c.bar(kBarInEmpty + st));
           if (V == kVarRowMajor) umma_commit(c.bar(kBarBEmpty + bs));
@@ -453,16 +437,19 @@ __device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, co
           tc_fence_after_sync();
           const uint32_t stage = c.sbase + p.sm_wring + ws * p.wstage_bytes;
           const uint32_t sbo = 16u * static_cast<uint32_t>(w);
-          for (int kk = k0; kk < k0 + w; kk += 16) {
-            const uint32_t kb = static_cast<uint32_t>(kk - k0) * 2u;
-            const uint64_t bd = smem_desc(stage + kb, sbo, swizzle_code(w));
-            const uint32_t acc = kk > 0 ? 1u : 0u;
-            if (l == 0)
-              umma_f16_ss(slot_tmem, smem_desc(in_base + aoff + kb, sbo, swizzle_code(w)), bd,
-                          li.idesc, acc);
-            else
-              umma_f16_ts(slot_tmem, slot_tmem + p.a_col + static_cast<uint32_t>(kk >> 1), bd,
-                          li.idesc, acc);
+          const uint32_t swc = swizzle_code(w);
+          if (l == 0) {
+            for (int kk = k0; kk < k0 + w; kk += 16) {
+              const uint32_t kb = static_cast<uint32_t>(kk - k0) * 2u;
+              umma_f16_ss(slot_tmem, smem_desc(in_base + aoff + kb, sbo, swc),
+                          smem_desc(stage + kb, sbo, swc), li.idesc, static_cast<uint32_t>(kk));
+            }
+          } else {
+            for (int kk = k0; kk < k0 + w; kk += 16) {
+              const uint32_t kb = static_cast<uint32_t>(kk - k0) * 2u;
+              umma_f16_ts(slot_tmem, slot_tmem + p.a_col + static_cast<uint32_t>(kk >> 1),
+                          smem_desc(stage + kb, sbo, swc), li.idesc, static_cast<uint32_t>(kk));
+            }
           }
           umma_commit(c.bar(kBarWEmpty + ws));
         } else {
@@ -502,40 +489,11 @@ __device__ __forceinline__ uint32_t out_chunk_off(int c0) {
   return static_cast<uint32_t>(c0 >> 5) * (kTileM * 64u);
 }
 
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, int w, uint32_t (&acc)[32]) {
-  if (w == 32)
-    tmem_ld_x32(taddr, acc);
-  else
-    tmem_ld_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(acc));
-}
-
-// Bias, rounding and activation of one chunk of w columns starting at c0,
-// then its stores: FP16 pairs into the slot's A region in TMEM (columns
-// c0/2 ..), or, after the last layer, 16-byte stores into the output staging
-// region of the chunk.
-template <int V>
-__device__ __forceinline__ void epilogue_store(const uint32_t (&acc)[32], int c0, int w, bool last,
-                                               __half2 slope2, uint32_t row, uint32_t out_dst,
-                                               uint32_t a_tmem) {
-  uint32_t h[16];
-  epilogue_chunk<V>(acc, w >> 1, !last, slope2, h);
-  if (last) {
-    const uint32_t base = out_dst + out_chunk_off(c0);
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc)
-      if (cc * 8 < w)
-        st_shared_v4_nc(base + swz(row * 2u * static_cast<uint32_t>(w) + cc * 16u, w), h[4 * cc],
-                        h[4 * cc + 1], h[4 * cc + 2], h[4 * cc + 3]);
-  } else if (w == 32) {
-    tmem_st_x16(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
-  } else {
-    tmem_st_x8(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
-  }
-}
-
 // Epilogue warp e serves tile slot e / (4G), column group (e % 4G) / 4 and
 // TMEM lane quadrant (warp index % 4), where G = 16 / (4 * slots) column
-// groups share the columns of a layer in 32-column chunks g, g + G, ...
+// groups share the columns of a layer in 32-column chunks g, g + G, ...; a
+// trailing 16-column chunk (N % 32 == 16) belongs to the group whose turn it
+// is.
 template <int V>
 __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c, int warp,
                                              int lane) {
@@ -552,71 +510,107 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
   const int n_out = p.dL;
   const bool storer = (lane == 0) && (32 * g < n_out);
   if (!warp_wait(c.bar(kBarWLoad), 0, p, c)) return;
+  const uint32_t tbase = c.tmem + lane_bits + static_cast<uint32_t>(s) * p.slot_cols;
   if (g == 0) {
     // The constant A slab of the bias MMA for layers read from TMEM: column 0
     // of every row holds (1.0, 0) as an FP16 pair, columns 1..7 zeros.
     const uint32_t ones[8] = {0x3C00u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    tmem_st_x8(c.tmem + lane_bits + static_cast<uint32_t>(s) * p.slot_cols + p.a_ones, ones);
+    tmem_st_x8(tbase + p.a_ones, ones);
     tmem_wait_st();
   }
-  const uint32_t tbase = c.tmem + lane_bits + static_cast<uint32_t>(s) * p.slot_cols;
+  const uint32_t a_tmem = tbase + p.a_col;
   for (int32_t r = 0; r * S + s < c.n_local; ++r) {
     const int32_t t = tile_of(r * S + s);
     bool ok = true;
-    for (int l = 0; l < L; ++l) {
+    // Hidden layers: accumulator -> FP16 -> activation -> next layer's A (TMEM).
+    for (int l = 0; l < L - 1; ++l) {
       const uint32_t q = static_cast<uint32_t>(r * L + l);
       if (!warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      const LayerRegs li = load_layer(p, c, l);
-      const int N = li.N;
-      const bool last = (l == L - 1);
+      const int N = load_layer(p, c, l).N;
+      for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
+        uint32_t acc[32], h[16];
+        tmem_ld_x32(tbase + static_cast<uint32_t>(c0), acc);
+        tmem_wait_ld();
+        convert_pairs<V, 16, true>(acc, slope2, h);
+        tmem_st_x16(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
+      }
+      if ((N & 31) && ((N >> 5) % G) == g) {
+        const int c0 = N - 16;
+        uint32_t acc[16], h[8];
+        tmem_ld_x16(tbase + static_cast<uint32_t>(c0), acc);
+        tmem_wait_ld();
+        convert_pairs<V, 8, true>(acc, slope2, h);
+        tmem_st_x8(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(c.bar(kBarActReady + s));
+    }
+    if (!ok) break;
+    // Last layer: accumulator -> FP16 -> output staging -> TMA store.
+    {
+      const int l = L - 1;
+      const uint32_t q = static_cast<uint32_t>(r * L + l);
+      if (!warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c)) break;
+      tc_fence_after_sync();
+      const int N = n_out;
       const uint32_t out_dst =
           c.sbase + p.sm_out +
           (static_cast<uint32_t>(s) * p.n_out_bufs + static_cast<uint32_t>(r) % p.n_out_bufs) *
               p.out_slot_bytes;
-      if (last) {
-        // This staging buffer went to this warp's TMA stores n_out_bufs tiles
-        // of this slot ago; they must have finished reading it.
-        if (storer) {
-          if (p.n_out_bufs > 1)
-            bulk_wait_group_read<1>();
-          else
-            bulk_wait_group_read<0>();
-        }
-        __syncwarp();
+      // This staging buffer went to this warp's TMA stores n_out_bufs tiles
+      // of this slot ago; they must have finished reading it.
+      if (storer) {
+        if (p.n_out_bufs > 1)
+          bulk_wait_group_read<1>();
+        else
+          bulk_wait_group_read<0>();
       }
-      // Chunks of this warp are 32 columns wide (a trailing one may be 16).
-      for (int c0 = 32 * g; c0 < N; c0 += 32 * G) {
-        const int w0 = (N - c0 >= 32) ? 32 : 16;
-        uint32_t acc[32];
-        tmem_ld_cols(tbase + static_cast<uint32_t>(c0), w0, acc);
+      __syncwarp();
+      for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
+        uint32_t acc[32], h[16];
+        tmem_ld_x32(tbase + static_cast<uint32_t>(c0), acc);
         tmem_wait_ld();
-        epilogue_store<V>(acc, c0, w0, last, slope2, row, out_dst, tbase + p.a_col);
+        convert_pairs<V, 16, false>(acc, slope2, h);
+        const uint32_t base = out_dst + out_chunk_off(c0);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          st_shared_v4_nc(base + swz(row * 64u + cc * 16u, 32), h[4 * cc], h[4 * cc + 1],
+                          h[4 * cc + 2], h[4 * cc + 3]);
       }
-      if (!last) tmem_wait_st();
+      if ((N & 31) && ((N >> 5) % G) == g) {
+        const int c0 = N - 16;
+        uint32_t acc[16], h[8];
+        tmem_ld_x16(tbase + static_cast<uint32_t>(c0), acc);
+        tmem_wait_ld();
+        convert_pairs<V, 8, false>(acc, slope2, h);
+        const uint32_t base = out_dst + out_chunk_off(c0);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+          st_shared_v4_nc(base + swz(row * 32u + cc * 16u, 16), h[4 * cc], h[4 * cc + 1],
+                          h[4 * cc + 2], h[4 * cc + 3]);
+      }
       tc_fence_before_sync();
-      if (last) fence_proxy_async_smem();  // staging tile -> TMA store (async proxy)
+      fence_proxy_async_smem();  // staging tile -> TMA store (async proxy)
       mbar_arrive(c.bar(kBarActReady + s));
-      if (last) {
-        __syncwarp();
-        if (storer) {
-          const int64_t row0 = static_cast<int64_t>(t) * kTileM + quad * 32;
-          if (row0 < p.n) {
-            for (int c0 = 32 * g; c0 < N; c0 += 32 * G) {
-              const int cols = (N - c0 >= 32) ? 32 : 16;
-              tma_store_2d(&p.tm_out[swizzle_kind(cols)],
-                           out_dst + out_chunk_off(c0) + static_cast<uint32_t>(quad * 32 * 2 * cols),
-                           c0, static_cast<int32_t>(row0));
-            }
+      __syncwarp();
+      if (storer) {
+        const int64_t row0 = static_cast<int64_t>(t) * kTileM + quad * 32;
+        if (row0 < p.n) {
+          for (int c0 = 32 * g; c0 < N; c0 += 32 * G) {
+            const int cols = (N - c0 >= 32) ? 32 : 16;
+            tma_store_2d(&p.tm_out[swizzle_kind(cols)],
+                         out_dst + out_chunk_off(c0) + static_cast<uint32_t>(quad * 32 * 2 * cols),
+                         c0, static_cast<int32_t>(row0));
           }
-          bulk_commit_group();
         }
+        bulk_commit_group();
       }
     }
-    if (!ok) break;
   }
   if (storer) bulk_wait_group_all();
 }

@@ -88,6 +88,16 @@ __device__ __forceinline__ uint4 ld_shared_u32x4(uint32_t addr) {
   return v;
 }
 
+// Load of shared data that never changes after the kernel's prologue (the
+// schedule table): not volatile, so the compiler may hoist and batch it.
+__device__ __forceinline__ uint4 ld_shared_const_u32x4(uint32_t addr) {
+  uint4 v;
+  asm("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
