@@ -8,20 +8,19 @@
 // accumulator and, beside it, the FP16 activations that feed the next layer
 // as the tensor core's A operand; only the input tile (layer 1's A), the
 // weights and the output staging live in shared memory. Roles, by warp:
-//   warp 0       producer: TMA loads of the [128 x d0] input tiles into a ring
-//                (and, in the row-major ablation, rebuilds the B operand of
-//                every layer of every tile from the row-major weights);
-//   warp 1       one thread issues the tcgen05.mma chains. For each layer it
-//                issues that layer for every slot before waiting on any slot's
-//                epilogue, so one slot's MMAs overlap the others' epilogues:
-//                D[128 x N] (FP32, TMEM) = A[128 x K] (FP16; smem for layer 1,
-//                TMEM after) * W^T (smem);
-//   warps 2..17  epilogue, 16 warps split as slots x 4 TMEM lane quadrants x
-//                column groups: tcgen05.ld of the accumulator rows, FP32 bias
-//                add, FP16 rounding, FP16 activation max(h, h*half(0.01)),
-//                tcgen05.st of the FP16 pairs into the slot's A region (or,
-//                after the last layer, 16-byte stores into an output staging
-//                tile that the same warp sends out by TMA).
+//   warps 0..3   control, one per slot: lane 0 keeps the slot's input ring
+//                filled by TMA and issues every layer's tcgen05.mma chain
+//                for the slot's tiles, D[128 x N] (FP32, TMEM) = A[128 x K]
+//                (FP16; smem for layer 1, TMEM after) * W^T (smem) + b; the
+//                four slots' chains run from four threads because one thread
+//                issues MMAs only about one per 60 cycles. (With streamed
+//                weights, the warp after the last slot's copies the weights.)
+//   warps 4..19  epilogue, 16 warps split as slots x 4 TMEM lane quadrants x
+//                column groups: tcgen05.ld of the accumulator rows, FP16
+//                rounding, FP16 activation max(h, h*half(0.01)), tcgen05.st
+//                of the FP16 pairs into the slot's A region (or, after the
+//                last layer, 16-byte stores into an output staging tile that
+//                the same warp sends out by TMA).
 //
 // The page "Profiling neural material inference" fixes the arithmetic
 // ("Experiment setup": the full layer chain per evaluation; "Bad versus good
@@ -30,8 +29,8 @@
 // rebuilt from row-major memory per tile) and the indexed-lane activation.
 //
 // All UMMA descriptors are precomputed on the host (the schedule) and copied
-// into shared memory once per CTA, so issuing one MMA is a 16-byte shared
-// load, two adds and the tcgen05.mma itself.
+// into shared memory once per CTA; a layer's chain loads its descriptors
+// together and issues its MMAs as one straight-line sequence.
 //
 // Every wait is bounded by a wall-clock limit. A wait that gives up sets the
 // device status word and a CTA-wide abort flag; every role then stops, waits
@@ -200,6 +199,70 @@ __device__ __forceinline__ void convert_pairs(const uint32_t* acc, __half2 slope
   }
 }
 
+// One layer's k-slab MMAs as a straight-line sequence: the NS descriptor
+// pairs are loaded from the shared schedule table together (one load latency
+// instead of one per MMA), then the NS tcgen05.mma follow back to back with
+// no branch between them. A single thread issues MMAs only about one per
+// 60 cycles and a dependent load or a branch before each adds to that, so
+// the chain is the slot's critical path.
+template <int NS>
+__device__ __forceinline__ void mma_seq_ss(uint32_t d, uint32_t tab, uint64_t a_add, uint64_t b_add,
+                                           uint32_t idesc) {
+  uint4 sd[NS];
+#pragma unroll
+  for (int k = 0; k < NS; ++k) sd[k] = ld_shared_const_u32x4(tab + 16u * k);
+#pragma unroll
+  for (int k = 0; k < NS; ++k)
+    umma_f16_ss(d, (static_cast<uint64_t>(sd[k].y) << 32 | sd[k].x) + a_add,
+                (static_cast<uint64_t>(sd[k].w) << 32 | sd[k].z) + b_add, idesc, k);
+}
+
+// Same with A in TMEM: k-slab k of the activations starts 8 columns (16 FP16
+// values per row) after slab k - 1.
+template <int NS>
+__device__ __forceinline__ void mma_seq_ts(uint32_t d, uint32_t a_tmem, uint32_t tab, uint64_t b_add,
+                                           uint32_t idesc) {
+  uint4 sd[NS];
+#pragma unroll
+  for (int k = 0; k < NS; ++k) sd[k] = ld_shared_const_u32x4(tab + 16u * k);
+#pragma unroll
+  for (int k = 0; k < NS; ++k)
+    umma_f16_ts(d, a_tmem + 8u * k, (static_cast<uint64_t>(sd[k].w) << 32 | sd[k].z) + b_add, idesc,
+                k);
+}
+
+// nslab = K / 16 is 1..16 (K <= 256); one switch picks the unrolled sequence.
+#define NM_SLAB_COUNTS(X) \
+  X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13) X(14) X(15) X(16)
+
+__device__ __forceinline__ void mma_chain_ss(uint32_t nslab, uint32_t d, uint32_t tab,
+                                             uint64_t a_add, uint64_t b_add, uint32_t idesc) {
+  switch (nslab) {
+#define NM_CASE(n) \
+  case n:          \
+    mma_seq_ss<n>(d, tab, a_add, b_add, idesc); \
+    break;
+    NM_SLAB_COUNTS(NM_CASE)
+#undef NM_CASE
+    default:
+      break;
+  }
+}
+
+__device__ __forceinline__ void mma_chain_ts(uint32_t nslab, uint32_t d, uint32_t a_tmem,
+                                             uint32_t tab, uint64_t b_add, uint32_t idesc) {
+  switch (nslab) {
+#define NM_CASE(n) \
+  case n:          \
+    mma_seq_ts<n>(d, a_tmem, tab, b_add, idesc); \
+    break;
+    NM_SLAB_COUNTS(NM_CASE)
+#undef NM_CASE
+    default:
+      break;
+  }
+}
+
 __device__ __forceinline__ void issue_input_tma(const FusedParams& p, uint32_t dst, uint32_t bar,
                                                 int32_t tile) {
   const int K = p.d0;
@@ -291,8 +354,6 @@ __device__ __forceinline__ void run_slot_control(const FusedParams& p, const Ctx
                           c.abort_flag, p.status);
         if (ok) {
           tc_fence_after_sync();
-          // The MMA sequences below are straight-line loops: a branch between
-          // two tcgen05.mma instructions roughly doubles their issue cost.
           const uint64_t b_add = b_base >> 4;
           const uint32_t slot_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
           const uint32_t nslab = li.slab_end - li.slab_begin;
@@ -301,22 +362,13 @@ __device__ __forceinline__ void run_slot_control(const FusedParams& p, const Ctx
           if (l == 0) {
             // Layer 1: A is the input tile in shared memory.
             const uint64_t a_add = (c.sbase + p.sm_in + st * p.in_stage_bytes) >> 4;
-            for (uint32_t k = 0; k < nslab; ++k) {
-              const uint4 sd = ld_shared_const_u32x4(tab + 16u * k);
-              umma_f16_ss(slot_tmem, (static_cast<uint64_t>(sd.y) << 32 | sd.x) + a_add,
-                          (static_cast<uint64_t>(sd.w) << 32 | sd.z) + b_add, li.idesc, k);
-            }
+            mma_chain_ss(nslab, slot_tmem, tab, a_add, b_add, li.idesc);
             // Bias: one more K=16 MMA, ones column x bias slab, added last.
             umma_f16_ss(slot_tmem, smem_desc(c.sbase + p.sm_ones, 256u, 6u), bias_bd, li.idesc, 1u);
           } else {
             // Later layers: A is the previous epilogue's FP16 output in TMEM,
             // 8 columns per 16-wide k-slab.
-            const uint32_t a_tmem = slot_tmem + p.a_col;
-            for (uint32_t k = 0; k < nslab; ++k) {
-              const uint4 sd = ld_shared_const_u32x4(tab + 16u * k);
-              umma_f16_ts(slot_tmem, a_tmem + 8u * k,
-                          (static_cast<uint64_t>(sd.w) << 32 | sd.z) + b_add, li.idesc, k);
-            }
+            mma_chain_ts(nslab, slot_tmem, slot_tmem + p.a_col, tab, b_add, li.idesc);
             umma_f16_ts(slot_tmem, slot_tmem + p.a_ones, bias_bd, li.idesc, 1u);
           }
           umma_commit(c.bar(kBarAccFull + s));
