@@ -110,8 +110,8 @@ WORKLOADS = {
         "page", (48, 64, 64, 64, 64, 64, 64, 64, 16), seed=1, n_unique=65536, repeats=16,
         description="page-shaped 48->64x7->16, 65,536 inputs x 16 = 1,048,576 evals, seed 1"),
     "ablation": Workload(
-        "ablation", (32, 32, 32, 32, 32, 32, 32, 32, 16), seed=0, n_unique=65536, repeats=16,
-        description="tiny network and inputs x 16 = 1,048,576 evals (layout/activation ablations)"),
+        "ablation", (48, 64, 64, 64, 64, 64, 64, 64, 16), seed=1, n_unique=65536, repeats=16,
+        description="the page-shaped network and inputs x 16 = 1,048,576 evals (layout/activation ablations)"),
     "wide": Workload(
         "wide", (64, 128, 128, 128, 128, 128, 128, 128, 16), seed=3, n_unique=16777216,
         description="64->128x7->16, 16,777,216 U(-1,1) inputs, one pass, seed 3"),
