@@ -137,6 +137,35 @@ nm_status nm_mlp_packed_blob(const nm_mlp *h, const void **blob);
  * A kernel-side wait that gives up is reported by nm_mlp_device_status. */
 nm_status nm_mlp_infer(nm_mlp *h, const void *in, int64_t n, void *out, nm_stream stream);
 
+/* The same evaluation with the inputs and outputs in HOST memory. The pages
+ * have no counterpart (their dispatch reads a batch already on the device);
+ * it serves callers whose samples live on the host, so that the copies in
+ * and out overlap the kernel instead of preceding and following it.
+ * host_in:  FP16 [n][dims[0]] row-major.  host_out: FP16 [n][dims[L]].
+ * Page-locked host memory (cudaHostAlloc / cudaHostRegister) lets the copies
+ * run asynchronously; pageable memory works but serialises them.
+ * The rows are processed in chunks (a multiple of 128 rows, see
+ * nm_mlp_set_host_chunk) on three streams the handle owns: chunk i's
+ * host-to-device copy, kernel and device-to-host copy run in order on
+ * stream i % 3, so the copies of neighbouring chunks overlap its kernel.
+ * Staging buffers for three chunks are allocated on the first call and kept
+ * by the handle. The work is ordered after everything already enqueued on
+ * `stream`, and `stream` waits for all of it: the host buffers must stay
+ * valid, and host_out must not be read, until `stream` reaches that point.
+ * Calls on one handle are serialised on its streams (safe, not concurrent).
+ * The results are bit-identical to nm_mlp_infer on the same rows.
+ * Errors: NM_ERR_INVALID_ARG (NULL pointer, n < 0 or n > 2^31 - 128),
+ * NM_ERR_NOT_PACKED, NM_ERR_UNSUPPORTED, NM_ERR_OOM (staging buffers),
+ * NM_ERR_CUDA. A kernel-side give-up is reported by nm_mlp_device_status. */
+nm_status nm_mlp_infer_host(nm_mlp *h, const void *host_in, int64_t n, void *host_out,
+                            nm_stream stream);
+
+/* Rows per chunk of nm_mlp_infer_host: a multiple of 128 in [128, 2^20], or
+ * 0 for the default (about 8 MiB of input per chunk, at least 16,384 rows).
+ * Changing it frees the staging buffers (after the handle's streams drain);
+ * the next call allocates them anew. Errors: NM_ERR_INVALID_ARG. */
+nm_status nm_mlp_set_host_chunk(nm_mlp *h, int64_t rows);
+
 /* Select the kernel variant used by later nm_mlp_infer calls.
  * Errors: NM_ERR_INVALID_ARG for an unknown variant. */
 nm_status nm_mlp_set_variant(nm_mlp *h, nm_variant v);

@@ -96,6 +96,15 @@ struct nm_mlp {
   const void* map_in = nullptr;
   const void* map_out = nullptr;
   int64_t map_n = -1;
+  // host-buffer pipeline (nm_mlp_infer_host)
+  int64_t host_chunk = 0;              // rows per chunk requested (0: default)
+  int64_t hs_rows = 0;                 // rows per chunk the staging buffers hold
+  size_t hs_in_bytes = 0;              // input part of one staging buffer (256-aligned)
+  size_t hs_each = 0;                  // bytes of one staging buffer
+  uint8_t* hs_stage = nullptr;         // kHostStreams staging buffers (device)
+  cudaStream_t hs[3] = {};
+  cudaEvent_t hs_start = nullptr;
+  cudaEvent_t hs_done[3] = {};
 };
 
 namespace {
@@ -104,6 +113,9 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kHostStreams = 3;
+constexpr int64_t kMaxRows = (static_cast<int64_t>(1) << 31) - 128;
 
 nm_status get_encoder() {
   std::call_once(g_encode_once, [] {
@@ -200,6 +212,68 @@ nm_status ensure_mirror(nm_mlp* h, cudaStream_t stream) {
   if (nm::launch_pack(pp, true, h->num_sms, stream) != cudaSuccess) return NM_ERR_CUDA;
   h->params.mirror = h->mirror;
   h->mirror_valid = true;
+  return NM_OK;
+}
+
+// Encodes the I/O tensor maps for (in, out, n) and launches the fused kernel
+// on `s`. Arguments are already checked.
+nm_status launch_infer(nm_mlp* h, const void* in, int64_t n, void* out, cudaStream_t s) {
+  nm_status st = encode_io_maps(h, in, out, n);
+  if (st != NM_OK) return st;
+  FusedParams& p = h->params;
+  p.n = n;
+  p.num_tiles = static_cast<int32_t>((n + nm::kTileM - 1) / nm::kTileM);
+  p.wait_ns = h->wait_ns;
+  p.test_stall = h->test_stall;
+  const uint32_t smem = nm::plan_fused_smem(p, h->dims, h->variant, h->smem_optin);
+  if (smem == 0) return NM_ERR_UNSUPPORTED;
+  const int grid = p.num_tiles < h->num_sms ? p.num_tiles : h->num_sms;
+  if (nm::launch_fused(p, h->variant, grid, smem, s) != cudaSuccess) return NM_ERR_CUDA;
+  return NM_OK;
+}
+
+// Staging buffers of the host-buffer pipeline: freed after the handle's
+// streams drain (cudaFree waits for the device anyway).
+void free_host_stage(nm_mlp* h) {
+  if (!h->hs_stage) return;
+  for (int i = 0; i < kHostStreams; ++i)
+    if (h->hs[i]) cudaStreamSynchronize(h->hs[i]);
+  cudaFree(h->hs_stage);
+  h->hs_stage = nullptr;
+  h->hs_rows = 0;
+}
+
+// Streams, events and staging buffers of nm_mlp_infer_host, created on first
+// use. Default chunk: about 8 MiB of input, at least 16,384 rows, at most
+// 2^20, a multiple of 128.
+nm_status ensure_host_pipeline(nm_mlp* h) {
+  if (!h->hs_start) {
+    for (int i = 0; i < kHostStreams; ++i) {
+      if (cudaStreamCreateWithFlags(&h->hs[i], cudaStreamNonBlocking) != cudaSuccess ||
+          cudaEventCreateWithFlags(&h->hs_done[i], cudaEventDisableTiming) != cudaSuccess)
+        return NM_ERR_CUDA;
+    }
+    if (cudaEventCreateWithFlags(&h->hs_start, cudaEventDisableTiming) != cudaSuccess) {
+      h->hs_start = nullptr;
+      return NM_ERR_CUDA;
+    }
+  }
+  if (h->hs_stage) return NM_OK;
+  int64_t rows = h->host_chunk;
+  if (rows == 0) {
+    rows = (static_cast<int64_t>(8) << 20) / (2 * h->dims[0]);
+    if (rows < 16384) rows = 16384;
+    if (rows > (static_cast<int64_t>(1) << 20)) rows = static_cast<int64_t>(1) << 20;
+    rows &= ~static_cast<int64_t>(nm::kTileM - 1);
+  }
+  const size_t in_bytes = (static_cast<size_t>(rows) * 2u * h->dims[0] + 255u) & ~size_t(255);
+  const size_t out_bytes = (static_cast<size_t>(rows) * 2u * h->dims[h->L] + 255u) & ~size_t(255);
+  void* p = nullptr;
+  if (cudaMalloc(&p, kHostStreams * (in_bytes + out_bytes)) != cudaSuccess) return NM_ERR_OOM;
+  h->hs_stage = static_cast<uint8_t*>(p);
+  h->hs_rows = rows;
+  h->hs_in_bytes = in_bytes;
+  h->hs_each = in_bytes + out_bytes;
   return NM_OK;
 }
 
@@ -360,7 +434,7 @@ nm_status nm_mlp_unpack_weights(const nm_mlp* h, void* const* W, void* const* b,
 
 nm_status nm_mlp_infer(nm_mlp* h, const void* in, int64_t n, void* out, nm_stream stream) {
   if (!h) return NM_ERR_INVALID_ARG;
-  if (n < 0 || n > (static_cast<int64_t>(1) << 31) - 128) return NM_ERR_INVALID_ARG;
+  if (n < 0 || n > kMaxRows) return NM_ERR_INVALID_ARG;
   if (n == 0) return NM_OK;
   if (!in || !out || !aligned16(in) || !aligned16(out)) return NM_ERR_INVALID_ARG;
   if (!h->packed) return NM_ERR_NOT_PACKED;
@@ -369,17 +443,61 @@ nm_status nm_mlp_infer(nm_mlp* h, const void* in, int64_t n, void* out, nm_strea
     const nm_status st = ensure_mirror(h, s);
     if (st != NM_OK) return st;
   }
-  nm_status st = encode_io_maps(h, in, out, n);
+  return launch_infer(h, in, n, out, s);
+}
+
+nm_status nm_mlp_infer_host(nm_mlp* h, const void* host_in, int64_t n, void* host_out,
+                            nm_stream stream) {
+  if (!h) return NM_ERR_INVALID_ARG;
+  if (n < 0 || n > kMaxRows) return NM_ERR_INVALID_ARG;
+  if (n == 0) return NM_OK;
+  if (!host_in || !host_out) return NM_ERR_INVALID_ARG;
+  if (!h->packed) return NM_ERR_NOT_PACKED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (h->variant == nm::kVarRowMajor) {
+    const nm_status st = ensure_mirror(h, s);
+    if (st != NM_OK) return st;
+  }
+  nm_status st = ensure_host_pipeline(h);
   if (st != NM_OK) return st;
-  FusedParams& p = h->params;
-  p.n = n;
-  p.num_tiles = static_cast<int32_t>((n + nm::kTileM - 1) / nm::kTileM);
-  p.wait_ns = h->wait_ns;
-  p.test_stall = h->test_stall;
-  const uint32_t smem = nm::plan_fused_smem(p, h->dims, h->variant, h->smem_optin);
-  if (smem == 0) return NM_ERR_UNSUPPORTED;
-  const int grid = p.num_tiles < h->num_sms ? p.num_tiles : h->num_sms;
-  if (nm::launch_fused(p, h->variant, grid, smem, s) != cudaSuccess) return NM_ERR_CUDA;
+  const size_t in_row = 2u * static_cast<size_t>(h->dims[0]);
+  const size_t out_row = 2u * static_cast<size_t>(h->dims[h->L]);
+  // The handle's streams start after the caller's prior work ...
+  if (cudaEventRecord(h->hs_start, s) != cudaSuccess) return NM_ERR_CUDA;
+  for (int i = 0; i < kHostStreams; ++i)
+    if (cudaStreamWaitEvent(h->hs[i], h->hs_start, 0) != cudaSuccess) return NM_ERR_CUDA;
+  // ... run the chunks: copy in, evaluate, copy out, each chunk in order on
+  // its stream, so neighbouring chunks overlap ...
+  int i = 0;
+  for (int64_t r0 = 0; r0 < n; r0 += h->hs_rows, i = (i + 1) % kHostStreams) {
+    const int64_t m = (n - r0 < h->hs_rows) ? (n - r0) : h->hs_rows;
+    uint8_t* din = h->hs_stage + static_cast<size_t>(i) * h->hs_each;
+    uint8_t* dout = din + h->hs_in_bytes;
+    const uint8_t* src = static_cast<const uint8_t*>(host_in) + static_cast<size_t>(r0) * in_row;
+    uint8_t* dst = static_cast<uint8_t*>(host_out) + static_cast<size_t>(r0) * out_row;
+    if (cudaMemcpyAsync(din, src, static_cast<size_t>(m) * in_row, cudaMemcpyHostToDevice,
+                        h->hs[i]) != cudaSuccess)
+      return NM_ERR_CUDA;
+    if ((st = launch_infer(h, din, m, dout, h->hs[i])) != NM_OK) return st;
+    if (cudaMemcpyAsync(dst, dout, static_cast<size_t>(m) * out_row, cudaMemcpyDeviceToHost,
+                        h->hs[i]) != cudaSuccess)
+      return NM_ERR_CUDA;
+  }
+  // ... and the caller's stream waits for all of them.
+  for (int k = 0; k < kHostStreams; ++k) {
+    if (cudaEventRecord(h->hs_done[k], h->hs[k]) != cudaSuccess) return NM_ERR_CUDA;
+    if (cudaStreamWaitEvent(s, h->hs_done[k], 0) != cudaSuccess) return NM_ERR_CUDA;
+  }
+  return NM_OK;
+}
+
+nm_status nm_mlp_set_host_chunk(nm_mlp* h, int64_t rows) {
+  if (!h) return NM_ERR_INVALID_ARG;
+  if (rows != 0 && (rows < nm::kTileM || rows > (static_cast<int64_t>(1) << 20) || rows % nm::kTileM))
+    return NM_ERR_INVALID_ARG;
+  if (rows == h->host_chunk) return NM_OK;
+  h->host_chunk = rows;
+  free_host_stage(h);
   return NM_OK;
 }
 
@@ -418,6 +536,12 @@ nm_status nm_mlp_set_test_stall(nm_mlp* h, int32_t enable) {
 void nm_mlp_destroy(nm_mlp* h) {
   if (!h) return;
   cudaDeviceSynchronize();
+  free_host_stage(h);
+  for (int i = 0; i < kHostStreams; ++i) {
+    if (h->hs[i]) cudaStreamDestroy(h->hs[i]);
+    if (h->hs_done[i]) cudaEventDestroy(h->hs_done[i]);
+  }
+  if (h->hs_start) cudaEventDestroy(h->hs_start);
   cudaFree(h->blob);
   cudaFree(h->status);
   cudaFree(h->sched);

@@ -37,6 +37,8 @@ SIGNATURES = {
     "nm_mlp_unpack_weights": (ctypes.c_int, [_P, _P, _P, _P]),
     "nm_mlp_packed_blob": (ctypes.c_int, [_P, ctypes.POINTER(_P)]),
     "nm_mlp_infer": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P, _P]),
+    "nm_mlp_infer_host": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P, _P]),
+    "nm_mlp_set_host_chunk": (ctypes.c_int, [_P, ctypes.c_int64]),
     "nm_mlp_set_variant": (ctypes.c_int, [_P, ctypes.c_int]),
     "nm_mlp_device_status": (ctypes.c_int, [_P, _P]),
     "nm_mlp_set_wait_limit": (ctypes.c_int, [_P, ctypes.c_uint64]),
@@ -173,6 +175,28 @@ class MLP:
             out = torch.empty((n, self.dims[-1]), dtype=torch.float16, device=x.device)
         _check(self.infer_raw(_addr(x), n, _addr(out), stream), "nm_mlp_infer")
         return out
+
+    def infer_host_raw(self, in_ptr: int, n: int, out_ptr: int, stream=None) -> int:
+        """nm_mlp_infer_host on raw host addresses; returns the status code."""
+        return lib().nm_mlp_infer_host(self._h, in_ptr, int(n), out_ptr, _stream(stream))
+
+    def infer_host(self, x, out=None, stream=None):
+        """out[n, d_L] = network(x[n, d_0]) with both FP16 tensors in host
+        memory (page-locked for overlapped copies). Asynchronous on `stream`:
+        synchronise it before reading `out`."""
+        import torch
+        if x.device.type != "cpu" or x.dtype != torch.float16 or not x.is_contiguous():
+            raise ValueError("infer_host wants a contiguous FP16 host tensor")
+        n = x.shape[0]
+        if out is None:
+            out = torch.empty((n, self.dims[-1]), dtype=torch.float16, pin_memory=True)
+        if out.device.type != "cpu" or out.dtype != torch.float16 or not out.is_contiguous():
+            raise ValueError("infer_host writes a contiguous FP16 host tensor")
+        _check(self.infer_host_raw(x.data_ptr(), n, out.data_ptr(), stream), "nm_mlp_infer_host")
+        return out
+
+    def set_host_chunk(self, rows: int):
+        _check(lib().nm_mlp_set_host_chunk(self._h, int(rows)), "nm_mlp_set_host_chunk")
 
     def set_variant(self, v: int):
         _check(lib().nm_mlp_set_variant(self._h, int(v)), "nm_mlp_set_variant")

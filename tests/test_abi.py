@@ -76,3 +76,9 @@ def test_noalloc_argument_checks_on_the_host(nmlib):
     assert L.nm_mlp_infer_noalloc(dims, 2, null2, null2, None, 4, None, None) == nmlib.NM_ERR_UNSUPPORTED
     dims = (ctypes.c_int32 * 2)(32, 16)
     assert L.nm_mlp_infer_noalloc(dims, 2, null2, null2, None, 4, None, None) == nmlib.NM_ERR_INVALID_ARG
+
+
+def test_host_path_argument_checks_on_the_host(nmlib):
+    L = nmlib.lib()
+    assert L.nm_mlp_infer_host(None, None, 4, None, None) == nmlib.NM_ERR_INVALID_ARG
+    assert L.nm_mlp_set_host_chunk(None, 0) == nmlib.NM_ERR_INVALID_ARG
