@@ -487,20 +487,39 @@ __device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, co
         if (!ok) break;
         if (has_tile) {
           tc_fence_after_sync();
+          // One K-segment: w / 16 k-slabs, 32 bytes apart in the segment's
+          // swizzle atom, so slab j's descriptors are the segment's plus 2j
+          // (start addresses are in 16-byte units). Issued straight-line.
           const uint32_t stage = c.sbase + p.sm_wring + ws * p.wstage_bytes;
           const uint32_t sbo = 16u * static_cast<uint32_t>(w);
           const uint32_t swc = swizzle_code(w);
+          const uint64_t bd = smem_desc(stage, sbo, swc);
+          const uint32_t acc0 = static_cast<uint32_t>(k0);  // first slab of the layer overwrites
           if (l == 0) {
-            for (int kk = k0; kk < k0 + w; kk += 16) {
-              const uint32_t kb = static_cast<uint32_t>(kk - k0) * 2u;
-              umma_f16_ss(slot_tmem, smem_desc(in_base + aoff + kb, sbo, swc),
-                          smem_desc(stage + kb, sbo, swc), li.idesc, static_cast<uint32_t>(kk));
+            const uint64_t ad = smem_desc(in_base + aoff, sbo, swc);
+            if (w == 64) {
+              umma_f16_ss(slot_tmem, ad, bd, li.idesc, acc0);
+              umma_f16_ss(slot_tmem, ad + 2u, bd + 2u, li.idesc, 1u);
+              umma_f16_ss(slot_tmem, ad + 4u, bd + 4u, li.idesc, 1u);
+              umma_f16_ss(slot_tmem, ad + 6u, bd + 6u, li.idesc, 1u);
+            } else if (w == 32) {
+              umma_f16_ss(slot_tmem, ad, bd, li.idesc, acc0);
+              umma_f16_ss(slot_tmem, ad + 2u, bd + 2u, li.idesc, 1u);
+            } else {
+              umma_f16_ss(slot_tmem, ad, bd, li.idesc, acc0);
             }
           } else {
-            for (int kk = k0; kk < k0 + w; kk += 16) {
-              const uint32_t kb = static_cast<uint32_t>(kk - k0) * 2u;
-              umma_f16_ts(slot_tmem, slot_tmem + p.a_col + static_cast<uint32_t>(kk >> 1),
-                          smem_desc(stage + kb, sbo, swc), li.idesc, static_cast<uint32_t>(kk));
+            const uint32_t at = slot_tmem + p.a_col + static_cast<uint32_t>(k0 >> 1);
+            if (w == 64) {
+              umma_f16_ts(slot_tmem, at, bd, li.idesc, acc0);
+              umma_f16_ts(slot_tmem, at + 8u, bd + 2u, li.idesc, 1u);
+              umma_f16_ts(slot_tmem, at + 16u, bd + 4u, li.idesc, 1u);
+              umma_f16_ts(slot_tmem, at + 24u, bd + 6u, li.idesc, 1u);
+            } else if (w == 32) {
+              umma_f16_ts(slot_tmem, at, bd, li.idesc, acc0);
+              umma_f16_ts(slot_tmem, at + 8u, bd + 2u, li.idesc, 1u);
+            } else {
+              umma_f16_ts(slot_tmem, at, bd, li.idesc, acc0);
             }
           }
           umma_commit(c.bar(kBarWEmpty + ws));
