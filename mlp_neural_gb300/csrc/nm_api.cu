@@ -93,9 +93,18 @@ struct nm_mlp {
   int device = 0;
   int num_sms = 0;
   uint32_t smem_optin = 0;
-  const void* map_in = nullptr;
-  const void* map_out = nullptr;
-  int64_t map_n = -1;
+  // I/O tensor maps of recent (in, out, n) triples, so that callers rotating
+  // among a few buffer sets do not re-encode them on every dispatch.
+  struct MapEntry {
+    CUtensorMap tm_in[3];
+    CUtensorMap tm_out[3];
+    const void* in = nullptr;
+    const void* out = nullptr;
+    int64_t n = -1;
+  };
+  static constexpr int kMapCache = 16;
+  MapEntry maps[kMapCache];
+  int map_next = 0;
   // host-buffer pipeline (nm_mlp_infer_host)
   int64_t host_chunk = 0;              // rows per chunk requested (0: default)
   int64_t hs_rows = 0;                 // rows per chunk the staging buffers hold
@@ -147,10 +156,17 @@ nm_status encode_map(CUtensorMap* m, const void* ptr, int width, int64_t rows, i
 }
 
 nm_status encode_io_maps(nm_mlp* h, const void* in, void* out, int64_t n) {
-  if (h->map_in == in && h->map_out == out && h->map_n == n) return NM_OK;
+  FusedParams& p = h->params;
+  for (int i = 0; i < nm_mlp::kMapCache; ++i) {
+    const nm_mlp::MapEntry& e = h->maps[i];
+    if (e.in == in && e.out == out && e.n == n) {
+      std::memcpy(p.tm_in, e.tm_in, sizeof(p.tm_in));
+      std::memcpy(p.tm_out, e.tm_out, sizeof(p.tm_out));
+      return NM_OK;
+    }
+  }
   nm_status st = get_encoder();
   if (st != NM_OK) return st;
-  FusedParams& p = h->params;
   std::memset(p.tm_in, 0, sizeof(p.tm_in));
   std::memset(p.tm_out, 0, sizeof(p.tm_out));
   int w[16], k0[16];
@@ -170,9 +186,13 @@ nm_status encode_io_maps(nm_mlp* h, const void* in, void* out, int64_t n) {
     st = encode_map(&p.tm_out[nm::swizzle_kind(16)], out, dl, n, 16, 32);
     if (st != NM_OK) return st;
   }
-  h->map_in = in;
-  h->map_out = out;
-  h->map_n = n;
+  nm_mlp::MapEntry& e = h->maps[h->map_next];
+  h->map_next = (h->map_next + 1) % nm_mlp::kMapCache;
+  std::memcpy(e.tm_in, p.tm_in, sizeof(p.tm_in));
+  std::memcpy(e.tm_out, p.tm_out, sizeof(p.tm_out));
+  e.in = in;
+  e.out = out;
+  e.n = n;
   return NM_OK;
 }
 
