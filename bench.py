@@ -376,7 +376,8 @@ def main(argv=None):
         achieved = w.hbm_bytes_per_eval * n / (avg_kernel_ms * 1e-3) / 1e9
         peak, unit = peaks["hbm_gbs"], "GB/s"
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": load_traffic(w.name, args.variant),
+                "frac": achieved / peak,
+                "traffic": None if args.evals else load_traffic(w.name, args.variant),
                 "kernel": "fused_mlp_kernel", "peak_source": (
                     f"{peaks_src}: " + ("dense bf16 burst (FP16 dense has the same nominal rate)"
                                         if bound == "tensor" else "HBM copy bandwidth"))}
