@@ -161,7 +161,7 @@ nm_status nm_mlp_infer_host(nm_mlp *h, const void *host_in, int64_t n, void *hos
                             nm_stream stream);
 
 /* Rows per chunk of nm_mlp_infer_host: a multiple of 128 in [128, 2^20], or
- * 0 for the default (about 8 MiB of input per chunk, at least 16,384 rows).
+ * 0 for the default (about 12 MiB of input per chunk, at least 16,384 rows).
  * Changing it frees the staging buffers (after the handle's streams drain);
  * the next call allocates them anew. Errors: NM_ERR_INVALID_ARG. */
 nm_status nm_mlp_set_host_chunk(nm_mlp *h, int64_t rows);

@@ -264,8 +264,9 @@ void free_host_stage(nm_mlp* h) {
 }
 
 // Streams, events and staging buffers of nm_mlp_infer_host, created on first
-// use. Default chunk: about 8 MiB of input, at least 16,384 rows, at most
-// 2^20, a multiple of 128.
+// use. Default chunk: about 12 MiB of input (large enough that the per-chunk
+// costs stay small, small enough that filling and draining the pipeline
+// stays short), at least 16,384 rows, at most 2^20, a multiple of 128.
 nm_status ensure_host_pipeline(nm_mlp* h) {
   if (!h->hs_start) {
     for (int i = 0; i < kHostStreams; ++i) {
@@ -281,7 +282,7 @@ nm_status ensure_host_pipeline(nm_mlp* h) {
   if (h->hs_stage) return NM_OK;
   int64_t rows = h->host_chunk;
   if (rows == 0) {
-    rows = (static_cast<int64_t>(8) << 20) / (2 * h->dims[0]);
+    rows = (static_cast<int64_t>(12) << 20) / (2 * h->dims[0]);
     if (rows < 16384) rows = 16384;
     if (rows > (static_cast<int64_t>(1) << 20)) rows = static_cast<int64_t>(1) << 20;
     rows &= ~static_cast<int64_t>(nm::kTileM - 1);

@@ -49,7 +49,7 @@ def test_host_path_bit_identical_to_device_path(dims, n, chunk):
 def test_host_path_default_chunk_many_chunks_and_oracle_sample(orc):
     import torch
     dims = synth.WORKLOADS["page"].dims
-    n = 3 * 87296 + 1000  # the default chunk for d0 = 48 is 87,296 rows
+    n = 3 * 131072 + 1000  # the default chunk for d0 = 48 is 131,072 rows
     W, b, x = synth.small_net_inputs(dims, seed=11, n=n)
     m = make_net(dims, W, b)
     ref = _device_path(m, x)
@@ -57,7 +57,7 @@ def test_host_path_default_chunk_many_chunks_and_oracle_sample(orc):
     torch.cuda.current_stream().synchronize()
     got = out.view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(got, ref)
-    rows = np.r_[0:64, 87296 - 3:87296 + 3, n - 64:n]
+    rows = np.r_[0:64, 131072 - 3:131072 + 3, n - 64:n]
     expect = orc.forward(dims, W, b, x[rows])
     assert_close(got[rows], expect)
     m.close()
