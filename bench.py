@@ -225,6 +225,30 @@ def run_reference(args, w, rank):
     return 0
 
 
+def rank_shard(w, rank: int):
+    """(first row, row count) of the synthetic input stream that `rank`
+    evaluates: every rank takes its own n_unique rows, so the ranks' shards
+    are disjoint and together are the first world * n_unique rows."""
+    return rank * w.n_unique, w.n_unique
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's `x` (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(evals_per_rank_step: int, steps: int, world: int, seconds: float) -> float:
+    """M evaluations per second of the whole job: every rank's evaluations
+    over the slowest rank's time."""
+    return evals_per_rank_step * steps * world / seconds / 1e6
+
+
 def workload_config(w):
     return {"workload": w.name, "dims": list(w.dims), "evals_per_step": w.n_evals,
             "unique_inputs": w.n_unique, "repeats": w.repeats, "seed": w.seed,
@@ -281,7 +305,7 @@ def main(argv=None):
     pack_ms = sorted(pack_ms)[len(pack_ms) // 2]
 
     # inputs: this rank's unique rows, repeated as the dispatch repeats them
-    xu = synth.inputs(w, rank * w.n_unique, w.n_unique)
+    xu = synth.inputs(w, *rank_shard(w, rank))
     xdev = to_dev(xu)
     if w.repeats > 1:
         xdev = xdev.repeat(w.repeats, 1)
@@ -331,13 +355,8 @@ def main(argv=None):
         raise RuntimeError("device status after the timed region")
     total_ms = ev0.elapsed_time(ev1)
     avg_kernel_ms = total_ms / K  # per dispatch, launch gaps included
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-
-    evals_all = w.n_evals * K * world
-    value = evals_all / (total_ms * 1e-3) / 1e6
+    total_ms = max_over_ranks(total_ms, world, dev)
+    value = whole_job_rate(w.n_evals, K, world, total_ms * 1e-3)
 
     # end to end through the C ABI's host-buffer call from pinned host
     # memory: every step copies its inputs in, evaluates and copies the
@@ -360,12 +379,8 @@ def main(argv=None):
     te0 = time.perf_counter()
     for _ in range(E):
         e2e_step()
-    te = time.perf_counter() - te0
-    if world > 1:
-        t = torch.tensor([te], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        te = float(t.item())
-    e2e_value = w.n_evals * E * world / te / 1e6
+    te = max_over_ranks(time.perf_counter() - te0, world, dev)
+    e2e_value = whole_job_rate(w.n_evals, E, world, te)
 
     peaks, peaks_src = load_peaks()
     bound, _, _ = roofline_bound(w, peaks)

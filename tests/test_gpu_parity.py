@@ -261,3 +261,26 @@ def test_full_wide_sampled(orc):
 
 def test_full_hetero_sampled(orc):
     _full_sampled(orc, "hetero")
+
+
+def test_many_rotating_buffer_sets(orc):
+    """More distinct (in, out) buffer pairs than the handle caches tensor maps
+    for: every dispatch must still read its own input and write its own
+    output."""
+    import torch
+    dims = (32, 48, 16)
+    n = 300
+    W, b, _ = synth.small_net_inputs(dims, seed=5, n=1)
+    m = make_net(dims, W, b)
+    sets = []
+    for i in range(20):
+        _, _, x = synth.small_net_inputs(dims, seed=100 + i, n=n)
+        sets.append((x, to_dev(x), torch.empty((n, dims[-1]), dtype=torch.float16, device="cuda")))
+    for rep in range(2):
+        for x, xd, od in sets:
+            m.infer(xd, od)
+    torch.cuda.synchronize()
+    assert m.device_status() == nm().NM_OK
+    for x, xd, od in sets:
+        assert_close(to_host(od), orc.forward(dims, W, b, x))
+    m.close()
