@@ -294,15 +294,24 @@ def main(argv=None):
     m.set_variant(VARIANTS[args.variant])
     m.pack_weights(Wd, bd, stream)
     torch.cuda.synchronize()
+    # one-time conversion cost: the device time of a conversion, from 20
+    # conversions captured in a CUDA graph and replayed between two events
+    # (so that the host's per-call overhead does not starve the device)
     pe0, pe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    with torch.cuda.graph(graph, stream=cap):
+        for _ in range(20):
+            m.pack_weights(Wd, bd, cap)
     pack_ms = []
-    for _ in range(5):
+    for _ in range(3):
         pe0.record(stream)
-        m.pack_weights(Wd, bd, stream)
+        graph.replay()
         pe1.record(stream)
         torch.cuda.synchronize()
-        pack_ms.append(pe0.elapsed_time(pe1))
-    pack_ms = sorted(pack_ms)[len(pack_ms) // 2]
+        pack_ms.append(pe0.elapsed_time(pe1) / 20)
+    pack_ms = sorted(pack_ms)[1]
+    del graph
 
     # inputs: this rank's unique rows, repeated as the dispatch repeats them
     xu = synth.inputs(w, *rank_shard(w, rank))
