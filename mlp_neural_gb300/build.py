@@ -23,8 +23,7 @@ LIB = os.path.join(PKG, "libnmmlp.so")
 SOURCES = ["nm_api.cu", "nm_fused.cu", "nm_noalloc.cu"]
 HEADERS = ["nm_internal.h", "nm_layout.cuh", "nm_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
-              "-diag-suppress", "177"]
+NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
 
 
 def _nvcc() -> str:

@@ -59,9 +59,6 @@ struct Ctx {
   __device__ __forceinline__ uint32_t bar(int i) const {
     return bars + static_cast<uint32_t>(i) * 8u;
   }
-  __device__ __forceinline__ const Schedule* sched(const FusedParams& p) const {
-    return reinterpret_cast<const Schedule*>(gbase + p.sm_sched);
-  }
   // Shared-window address of field `off` of layer l's LayerInfo.
   __device__ __forceinline__ uint32_t layer_addr(const FusedParams& p, int l) const {
     return sbase + p.sm_sched + static_cast<uint32_t>(l) * static_cast<uint32_t>(sizeof(LayerInfo));
@@ -74,6 +71,10 @@ struct Ctx {
 
 __host__ __device__ constexpr bool is_scalar_act(int V) {
   return V == kVarScalar || V == kVarScalarStream;
+}
+
+__host__ __device__ constexpr bool is_stream(int V) {
+  return V == kVarFusedStream || V == kVarScalarStream;
 }
 
 // LayerInfo as loaded from shared memory (two 16-byte loads).
@@ -401,8 +402,6 @@ __device__ __forceinline__ void run_slot_control(const FusedParams& p, const Ctx
 // segment) in which every slot's control thread consumes them. A stage is
 // released once every slot's MMAs on it have completed (or, for a slot with
 // no tile in that round, once it has seen the stage).
-
-__device__ __forceinline__ bool is_stream(int V) { return V == kVarFusedStream || V == kVarScalarStream; }
 
 __device__ __forceinline__ void run_weight_producer(const FusedParams& p, const Ctx& c) {
   const int32_t S = static_cast<int32_t>(p.n_slots);
@@ -763,7 +762,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   if (warp == 0 && lane == 0) {
     // Stage the schedule (and the packed weight images) once for the whole
     // persistent loop.
-    const uint32_t wbytes = (V == kVarRowMajor || is_stream(V)) ? 0u : p.bias_off;
+    uint32_t wbytes = 0;  // resident weight images, if any
+    if constexpr (V != kVarRowMajor && !is_stream(V)) wbytes = p.bias_off;
     mbar_arrive_expect_tx(c.bar(kBarWLoad), p.sched_bytes + wbytes);
     bulk_load(c.sbase + p.sm_sched, p.sched, p.sched_bytes, c.bar(kBarWLoad));
     for (uint32_t off = 0; off < wbytes; off += 32768u) {
