@@ -284,3 +284,51 @@ def test_many_rotating_buffer_sets(orc):
     for x, xd, od in sets:
         assert_close(to_host(od), orc.forward(dims, W, b, x))
     m.close()
+
+
+def test_infer_captured_in_cuda_graph(orc):
+    """nm_mlp_infer is capturable: a graph replays the dispatch on new input
+    contents written into the same buffers."""
+    import torch
+    dims = synth.WORKLOADS["page"].dims
+    n = 1000
+    W, b, x1 = synth.small_net_inputs(dims, seed=21, n=n)
+    _, _, x2 = synth.small_net_inputs(dims, seed=22, n=n)
+    m = make_net(dims, W, b)
+    xd = to_dev(x1)
+    od = torch.empty((n, dims[-1]), dtype=torch.float16, device="cuda")
+    m.infer(xd, od)  # one eager dispatch first (one-time launch set-up)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        m.infer(xd, od, stream=side)
+    for x in (x1, x2):
+        xd.copy_(to_dev(x))
+        od.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_close(to_host(od), orc.forward(dims, W, b, x))
+    assert m.device_status() == nm().NM_OK
+    m.close()
+
+
+def test_two_handles_on_two_streams(orc):
+    """Two networks dispatched concurrently on two streams do not disturb
+    each other."""
+    import torch
+    nets = []
+    for seed, dims in ((31, (32, 64, 16)), (32, synth.WORKLOADS["page"].dims)):
+        W, b, x = synth.small_net_inputs(dims, seed=seed, n=5000)
+        m = make_net(dims, W, b)
+        out = torch.empty((5000, dims[-1]), dtype=torch.float16, device="cuda")
+        nets.append((dims, W, b, x, m, to_dev(x), out, torch.cuda.Stream()))
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for dims, W, b, x, m, xd, out, st in nets:
+            m.infer(xd, out, stream=st)
+    torch.cuda.synchronize()
+    for dims, W, b, x, m, xd, out, st in nets:
+        assert m.device_status() == nm().NM_OK
+        assert_close(to_host(out), orc.forward(dims, W, b, x))
+        m.close()
