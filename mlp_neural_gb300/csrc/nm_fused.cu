@@ -449,7 +449,9 @@ __device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, co
   if (p.test_stall) ok = wait_phase(c.bar(kBarNever), 0, p.wait_ns, c.abort_flag, p.status);
   if (ok) ok = wait_phase(c.bar(kBarWLoad), 0, p.wait_ns, c.abort_flag, p.status);
   const uint32_t slot_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
-  uint32_t g = 0;  // weight stages consumed
+  // Weight ring position, kept incrementally (no division on the critical
+  // path): the next stage to consume and the parity of its current fill.
+  uint32_t ws = 0, wph = 0;
   for (int32_t r = 0; r < n_rounds_all && ok; ++r) {
     const bool has_tile = r < n_rounds;
     while (ok && has_tile && issued + 1 < r + static_cast<int32_t>(D) && issued + 1 < n_rounds) {
@@ -464,8 +466,13 @@ __device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, co
       issued = static_cast<int32_t>(rr);
     }
     const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(r) % D;
+    const uint32_t in_base = c.sbase + p.sm_in + st * p.in_stage_bytes;
     for (int l = 0; l < L && ok; ++l) {
       const LayerRegs li = load_layer(p, c, l);
+      // The first K-segment's geometry, computed before the wait.
+      uint32_t aoff;
+      int w, k0;
+      locate(kTileM, li.K, 0, aoff, w, k0);
       if (has_tile) {
         const int32_t q = r * L + l - 1;
         if (q >= 0)
@@ -475,14 +482,9 @@ __device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, co
           ok = wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(r) / D) & 1u, p.wait_ns,
                           c.abort_flag, p.status);
       }
-      const uint32_t in_base = c.sbase + p.sm_in + st * p.in_stage_bytes;
       for (int k = 0; k < li.K && ok;) {
-        uint32_t boff, aoff;
-        int w, k0;
-        locate(static_cast<uint32_t>(li.N), li.K, k, boff, w, k0);
-        locate(kTileM, li.K, k, aoff, w, k0);
-        const uint32_t ws = g % RW;
-        ok = wait_phase(c.bar(kBarWFull + ws), (g / RW) & 1u, p.wait_ns, c.abort_flag, p.status);
+        if (k > 0) locate(kTileM, li.K, k, aoff, w, k0);
+        ok = wait_phase(c.bar(kBarWFull + ws), wph, p.wait_ns, c.abort_flag, p.status);
         if (!ok) break;
         if (has_tile) {
           tc_fence_after_sync();
@@ -525,7 +527,10 @@ __device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, co
         } else {
           mbar_arrive(c.bar(kBarWEmpty + ws));
         }
-        ++g;
+        if (++ws == RW) {
+          ws = 0;
+          wph ^= 1u;
+        }
         k = k0 + w;
       }
       if (ok && has_tile) {
