@@ -346,6 +346,14 @@ __device__ __forceinline__ void run_slot_control(const FusedParams& p, const Ctx
         __syncwarp();
       }
       if (lane == 0) {
+        // Everything the MMA issue needs is computed before the wait, so that
+        // the MMAs follow the wake-up directly.
+        const uint64_t b_add = b_base >> 4;
+        const uint32_t slot_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
+        const uint32_t nslab = li.slab_end - li.slab_begin;
+        const uint32_t tab = c.slab_addr(p, li.slab_begin);
+        const uint64_t bias_bd = smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u);
+        const uint64_t a_add = (c.sbase + p.sm_in + st * p.in_stage_bytes) >> 4;
         const int32_t q = r * L + l - 1;  // completion of this slot's previous epilogue
         if (q >= 0)
           ok = spin_phase(c.bar(kBarActReady + s), static_cast<uint32_t>(q) & 1u, p.wait_ns,
@@ -355,14 +363,8 @@ __device__ __forceinline__ void run_slot_control(const FusedParams& p, const Ctx
                           c.abort_flag, p.status);
         if (ok) {
           tc_fence_after_sync();
-          const uint64_t b_add = b_base >> 4;
-          const uint32_t slot_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
-          const uint32_t nslab = li.slab_end - li.slab_begin;
-          const uint32_t tab = c.slab_addr(p, li.slab_begin);
-          const uint64_t bias_bd = smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u);
           if (l == 0) {
             // Layer 1: A is the input tile in shared memory.
-            const uint64_t a_add = (c.sbase + p.sm_in + st * p.in_stage_bytes) >> 4;
             mma_chain_ss(nslab, slot_tmem, tab, a_add, b_add, li.idesc);
             // Bias: one more K=16 MMA, ones column x bias slab, added last.
             umma_f16_ss(slot_tmem, smem_desc(c.sbase + p.sm_ones, 256u, 6u), bias_bd, li.idesc, 1u);
