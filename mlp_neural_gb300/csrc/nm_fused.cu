@@ -202,65 +202,79 @@ __device__ __forceinline__ void convert_pairs(const uint32_t* acc, __half2 slope
 
 // One layer's k-slab MMAs as a straight-line sequence: the NS descriptor
 // pairs are loaded from the shared schedule table together (one load latency
-// instead of one per MMA), then the NS tcgen05.mma follow back to back with
+// instead of one per MMA) -- before `wait` runs, since the table is constant --
+// then, once `wait` has succeeded, the NS tcgen05.mma follow back to back with
 // no branch between them. A single thread issues MMAs only about one per
 // 60 cycles and a dependent load or a branch before each adds to that, so
-// the chain is the slot's critical path.
-template <int NS>
-__device__ __forceinline__ void mma_seq_ss(uint32_t d, uint32_t tab, uint64_t a_add, uint64_t b_add,
-                                           uint32_t idesc) {
+// the chain is the slot's critical path. Returns false if `wait` gave up.
+template <int NS, class Wait>
+__device__ __forceinline__ bool mma_seq_ss(uint32_t d, uint32_t tab, uint64_t a_add, uint64_t b_add,
+                                           uint32_t idesc, Wait&& wait) {
+  // Up to 8 descriptor pairs are fetched before the wait (register budget);
+  // the rest, together, right after it.
+  constexpr int kPre = NS < 8 ? NS : 8;
   uint4 sd[NS];
 #pragma unroll
-  for (int k = 0; k < NS; ++k) sd[k] = ld_shared_const_u32x4(tab + 16u * k);
+  for (int k = 0; k < kPre; ++k) sd[k] = ld_shared_u32x4_ordered(tab + 16u * k);
+  if (!wait()) return false;
+#pragma unroll
+  for (int k = kPre; k < NS; ++k) sd[k] = ld_shared_u32x4_ordered(tab + 16u * k);
+  tc_fence_after_sync();
 #pragma unroll
   for (int k = 0; k < NS; ++k)
     umma_f16_ss(d, (static_cast<uint64_t>(sd[k].y) << 32 | sd[k].x) + a_add,
                 (static_cast<uint64_t>(sd[k].w) << 32 | sd[k].z) + b_add, idesc, k);
+  return true;
 }
 
 // Same with A in TMEM: k-slab k of the activations starts 8 columns (16 FP16
-// values per row) after slab k - 1.
-template <int NS>
-__device__ __forceinline__ void mma_seq_ts(uint32_t d, uint32_t a_tmem, uint32_t tab, uint64_t b_add,
-                                           uint32_t idesc) {
-  uint4 sd[NS];
+// values per row) after slab k - 1; only the B descriptors are fetched.
+template <int NS, class Wait>
+__device__ __forceinline__ bool mma_seq_ts(uint32_t d, uint32_t a_tmem, uint32_t tab, uint64_t b_add,
+                                           uint32_t idesc, Wait&& wait) {
+  uint2 bd[NS];
 #pragma unroll
-  for (int k = 0; k < NS; ++k) sd[k] = ld_shared_const_u32x4(tab + 16u * k);
+  for (int k = 0; k < NS; ++k) bd[k] = ld_shared_u32x2_ordered(tab + 16u * k + 8u);
+  if (!wait()) return false;
+  tc_fence_after_sync();
 #pragma unroll
   for (int k = 0; k < NS; ++k)
-    umma_f16_ts(d, a_tmem + 8u * k, (static_cast<uint64_t>(sd[k].w) << 32 | sd[k].z) + b_add, idesc,
+    umma_f16_ts(d, a_tmem + 8u * k, (static_cast<uint64_t>(bd[k].y) << 32 | bd[k].x) + b_add, idesc,
                 k);
+  return true;
 }
 
 // nslab = K / 16 is 1..16 (K <= 256); one switch picks the unrolled sequence.
 #define NM_SLAB_COUNTS(X) \
   X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13) X(14) X(15) X(16)
 
-__device__ __forceinline__ void mma_chain_ss(uint32_t nslab, uint32_t d, uint32_t tab,
-                                             uint64_t a_add, uint64_t b_add, uint32_t idesc) {
+template <class Wait>
+__device__ __forceinline__ bool mma_chain_ss(uint32_t nslab, uint32_t d, uint32_t tab,
+                                             uint64_t a_add, uint64_t b_add, uint32_t idesc,
+                                             Wait&& wait) {
   switch (nslab) {
 #define NM_CASE(n) \
   case n:          \
-    mma_seq_ss<n>(d, tab, a_add, b_add, idesc); \
-    break;
+    return mma_seq_ss<n>(d, tab, a_add, b_add, idesc, wait);
     NM_SLAB_COUNTS(NM_CASE)
 #undef NM_CASE
     default:
-      break;
+      return false;
   }
 }
 
-__device__ __forceinline__ void mma_chain_ts(uint32_t nslab, uint32_t d, uint32_t a_tmem,
-                                             uint32_t tab, uint64_t b_add, uint32_t idesc) {
+template <class Wait>
+__device__ __forceinline__ bool mma_chain_ts(uint32_t nslab, uint32_t d, uint32_t a_tmem,
+                                             uint32_t tab, uint64_t b_add, uint32_t idesc,
+                                             Wait&& wait) {
   switch (nslab) {
 #define NM_CASE(n) \
   case n:          \
-    mma_seq_ts<n>(d, a_tmem, tab, b_add, idesc); \
-    break;
+    return mma_seq_ts<n>(d, a_tmem, tab, b_add, idesc, wait);
     NM_SLAB_COUNTS(NM_CASE)
 #undef NM_CASE
     default:
-      break;
+      return false;
   }
 }
 
@@ -355,25 +369,29 @@ __device__ __forceinline__ void run_slot_control(const FusedParams& p, const Ctx
         const uint64_t bias_bd = smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u);
         const uint64_t a_add = (c.sbase + p.sm_in + st * p.in_stage_bytes) >> 4;
         const int32_t q = r * L + l - 1;  // completion of this slot's previous epilogue
-        if (q >= 0)
-          ok = spin_phase(c.bar(kBarActReady + s), static_cast<uint32_t>(q) & 1u, p.wait_ns,
-                          c.abort_flag, p.status);
-        if (ok && l == 0)
-          ok = wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(r) / D) & 1u, p.wait_ns,
-                          c.abort_flag, p.status);
-        if (ok) {
-          tc_fence_after_sync();
-          if (l == 0) {
-            // Layer 1: A is the input tile in shared memory.
-            mma_chain_ss(nslab, slot_tmem, tab, a_add, b_add, li.idesc);
-            // Bias: one more K=16 MMA, ones column x bias slab, added last.
+        auto wait = [&]() -> bool {
+          bool w_ok = true;
+          if (q >= 0)
+            w_ok = spin_phase(c.bar(kBarActReady + s), static_cast<uint32_t>(q) & 1u, p.wait_ns,
+                              c.abort_flag, p.status);
+          if (w_ok && l == 0)
+            w_ok = wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(r) / D) & 1u,
+                              p.wait_ns, c.abort_flag, p.status);
+          return w_ok;
+        };
+        if (l == 0) {
+          // Layer 1: A is the input tile in shared memory.
+          ok = mma_chain_ss(nslab, slot_tmem, tab, a_add, b_add, li.idesc, wait);
+          // Bias: one more K=16 MMA, ones column x bias slab, added last.
+          if (ok)
             umma_f16_ss(slot_tmem, smem_desc(c.sbase + p.sm_ones, 256u, 6u), bias_bd, li.idesc, 1u);
-          } else {
-            // Later layers: A is the previous epilogue's FP16 output in TMEM,
-            // 8 columns per 16-wide k-slab.
-            mma_chain_ts(nslab, slot_tmem, slot_tmem + p.a_col, tab, b_add, li.idesc);
-            umma_f16_ts(slot_tmem, slot_tmem + p.a_ones, bias_bd, li.idesc, 1u);
-          }
+        } else {
+          // Later layers: A is the previous epilogue's FP16 output in TMEM,
+          // 8 columns per 16-wide k-slab.
+          ok = mma_chain_ts(nslab, slot_tmem, slot_tmem + p.a_col, tab, b_add, li.idesc, wait);
+          if (ok) umma_f16_ts(slot_tmem, slot_tmem + p.a_ones, bias_bd, li.idesc, 1u);
+        }
+        if (ok) {
           umma_commit(c.bar(kBarAccFull + s));
           if (l == 0) umma_commit(c.bar(kBarInEmpty + st));
           if (V == kVarRowMajor) umma_commit(c.bar(kBarBEmpty + bs));

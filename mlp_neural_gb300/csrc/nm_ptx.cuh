@@ -98,6 +98,23 @@ __device__ __forceinline__ uint4 ld_shared_const_u32x4(uint32_t addr) {
   return v;
 }
 
+// 16-byte shared load kept in program order with the surrounding volatile
+// asm (waits, MMAs): for data that is constant but must be fetched before a
+// wait rather than after it.
+__device__ __forceinline__ uint4 ld_shared_u32x4_ordered(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint2 ld_shared_u32x2_ordered(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
