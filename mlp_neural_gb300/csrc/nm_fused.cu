@@ -620,12 +620,12 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
     // Hidden layers: accumulator -> FP16 -> activation -> next layer's A (TMEM).
     for (int l = 0; l < L - 1; ++l) {
       const uint32_t q = static_cast<uint32_t>(r * L + l);
+      const int N = load_layer(p, c, l).N;  // fetched before the wait
       if (!warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      const int N = load_layer(p, c, l).N;
       for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
         uint32_t acc[32], h[16];
         tmem_ld_x32(tbase + static_cast<uint32_t>(c0), acc);
@@ -650,15 +650,14 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
     {
       const int l = L - 1;
       const uint32_t q = static_cast<uint32_t>(r * L + l);
-      if (!warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c)) break;
-      tc_fence_after_sync();
       const int N = n_out;
       const uint32_t out_dst =
           c.sbase + p.sm_out +
           (static_cast<uint32_t>(s) * p.n_out_bufs + static_cast<uint32_t>(r) % p.n_out_bufs) *
               p.out_slot_bytes;
       // This staging buffer went to this warp's TMA stores n_out_bufs tiles
-      // of this slot ago; they must have finished reading it.
+      // of this slot ago; they must have finished reading it (checked before
+      // the accumulator wait, which it does not depend on).
       if (storer) {
         if (p.n_out_bufs > 1)
           bulk_wait_group_read<1>();
@@ -666,6 +665,8 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
           bulk_wait_group_read<0>();
       }
       __syncwarp();
+      if (!warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c)) break;
+      tc_fence_after_sync();
       for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
         uint32_t acc[32], h[16];
         tmem_ld_x32(tbase + static_cast<uint32_t>(c0), acc);
