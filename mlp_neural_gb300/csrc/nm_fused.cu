@@ -4,23 +4,30 @@
 // and runs every layer of the network on each tile without leaving the SM
 // ("Optimization Techniques: Squeezing the Silicon", "Kernel Fusion": one
 // write to memory, intermediates stay on chip). Up to four tiles are in
-// flight per CTA (tile slots). A slot owns a TMEM region holding its FP32
-// accumulator and, beside it, the FP16 activations that feed the next layer
-// as the tensor core's A operand; only the input tile (layer 1's A), the
-// weights and the output staging live in shared memory. Roles, by warp:
-//   warps 0..3   control, one per slot: lane 0 keeps the slot's input ring
-//                filled by TMA and issues every layer's tcgen05.mma chain
-//                for the slot's tiles, D[128 x N] (FP32, TMEM) = A[128 x K]
-//                (FP16; smem for layer 1, TMEM after) * W^T (smem) + b; the
-//                four slots' chains run from four threads because one thread
-//                issues MMAs only about one per 60 cycles. (With streamed
-//                weights, the warp after the last slot's copies the weights.)
+// flight per CTA (tile slots). A slot owns two TMEM regions, each as wide as
+// the widest layer: the slot's q-th layer evaluation (chain q) accumulates in
+// FP32 in region q & 1, and its epilogue writes the FP16 activations -- the
+// next layer's A operand -- back into the columns of that region it has just
+// read, while chain q + 1 accumulates in the other region. Only the input
+// tile (layer 1's A), the weights, the bias operands and the output staging
+// live in shared memory. Roles, by warp:
+//   warps 0..3   control, one per slot: lane 0 issues every layer's
+//                tcgen05.mma chain for the slot's tiles, D[128 x N] (FP32,
+//                TMEM) = A[128 x K] (FP16; smem for layer 1, TMEM after) *
+//                W^T (smem) + b; the four slots' chains run from four threads
+//                because one thread issues MMAs only about one per 60 cycles.
+//                (With streamed weights, the warp after the last slot's
+//                copies the weights.)
 //   warps 4..19  epilogue, 16 warps split as slots x 4 TMEM lane quadrants x
 //                column groups: tcgen05.ld of the accumulator rows, FP16
 //                rounding, FP16 activation max(h, h*half(0.01)), tcgen05.st
-//                of the FP16 pairs into the slot's A region (or, after the
-//                last layer, 16-byte stores into an output staging tile that
-//                the same warp sends out by TMA).
+//                of the FP16 pairs (or, after the last layer, 16-byte stores
+//                into an output staging tile that the same warp sends out by
+//                TMA). The epilogue reports its first half of the columns
+//                separately, so the next layer's MMAs on those k-slabs start
+//                while it works on the second half.
+//   warp 20      input producer: lane 0 keeps every slot's input ring filled
+//                by TMA, off the control threads' critical path.
 //
 // The page "Profiling neural material inference" fixes the arithmetic
 // ("Experiment setup": the full layer chain per evaluation; "Bad versus good
@@ -30,7 +37,7 @@
 //
 // All UMMA descriptors are precomputed on the host (the schedule) and copied
 // into shared memory once per CTA; a layer's chain loads its descriptors
-// together and issues its MMAs as one straight-line sequence.
+// together and issues its MMAs as straight-line sequences.
 //
 // Every wait is bounded by a wall-clock limit. A wait that gives up sets the
 // device status word and a CTA-wide abort flag; every role then stops, waits
@@ -96,6 +103,12 @@ __device__ __forceinline__ LayerRegs load_layer(const FusedParams& p, const Ctx&
   r.rm_off = y.z;
   r.w_off = y.w;
   return r;
+}
+
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.b32 %0, 1, 0, P;\n\t}" : "=r"(pred));
+  return pred != 0;
 }
 
 // Bounded wait on an mbarrier phase. Gives up (and raises the abort flag and
@@ -227,21 +240,25 @@ __device__ __forceinline__ bool mma_seq_ss(uint32_t d, uint32_t tab, uint64_t a_
   return true;
 }
 
-// Same with A in TMEM: k-slab k of the activations starts 8 columns (16 FP16
-// values per row) after slab k - 1; only the B descriptors are fetched.
-template <int NS, class Wait>
-__device__ __forceinline__ bool mma_seq_ts(uint32_t d, uint32_t a_tmem, uint32_t tab, uint64_t b_add,
-                                           uint32_t idesc, Wait&& wait) {
+// Column of k-slab k of a layer's A operand inside the previous chain's
+// region (streamed-weight layout): the epilogue writes the 16 FP16 pairs of
+// accumulator chunk c (columns [32c, 32c + 32)) into the chunk's own first
+// 16 columns, slab 2c first, so slab k starts at 32 (k >> 1) + 8 (k & 1).
+__host__ __device__ constexpr uint32_t a_slab_col(uint32_t k) { return 32u * (k >> 1) + 8u * (k & 1u); }
+
+// Same with A in TMEM (resident-weight layout: k-slab k of the activations
+// starts 8 columns, 16 FP16 values per row, after slab k - 1); only the B
+// descriptors are fetched.
+template <int NS>
+__device__ __forceinline__ void mma_seq_ts(uint32_t d, uint32_t a_tmem, uint32_t tab, uint64_t b_add,
+                                           uint32_t idesc) {
   uint2 bd[NS];
 #pragma unroll
   for (int k = 0; k < NS; ++k) bd[k] = ld_shared_u32x2_ordered(tab + 16u * k + 8u);
-  if (!wait()) return false;
-  tc_fence_after_sync();
 #pragma unroll
   for (int k = 0; k < NS; ++k)
     umma_f16_ts(d, a_tmem + 8u * k, (static_cast<uint64_t>(bd[k].y) << 32 | bd[k].x) + b_add, idesc,
                 k);
-  return true;
 }
 
 // nslab = K / 16 is 1..16 (K <= 256); one switch picks the unrolled sequence.
@@ -263,18 +280,17 @@ __device__ __forceinline__ bool mma_chain_ss(uint32_t nslab, uint32_t d, uint32_
   }
 }
 
-template <class Wait>
-__device__ __forceinline__ bool mma_chain_ts(uint32_t nslab, uint32_t d, uint32_t a_tmem,
-                                             uint32_t tab, uint64_t b_add, uint32_t idesc,
-                                             Wait&& wait) {
+__device__ __forceinline__ void mma_chain_ts(uint32_t nslab, uint32_t d, uint32_t a_tmem,
+                                             uint32_t tab, uint64_t b_add, uint32_t idesc) {
   switch (nslab) {
 #define NM_CASE(n) \
   case n:          \
-    return mma_seq_ts<n>(d, a_tmem, tab, b_add, idesc, wait);
+    mma_seq_ts<n>(d, a_tmem, tab, b_add, idesc); \
+    break;
     NM_SLAB_COUNTS(NM_CASE)
 #undef NM_CASE
     default:
-      return false;
+      break;
   }
 }
 
@@ -294,124 +310,269 @@ __device__ __forceinline__ int32_t tile_of(int32_t i) {
   return static_cast<int32_t>(blockIdx.x) + i * static_cast<int32_t>(gridDim.x);
 }
 
-// ------------------------------------------------------------------ slot control
-// Control warp of tile slot s (warp index s). Its lane 0 keeps the slot's own
-// input ring (p.n_in_stages stages, rounds r, r+1, ... of this slot) filled by
-// TMA and issues every layer's tcgen05.mma chain for the slot's tiles; the
-// four slots' chains run in four warps, so their issue latencies overlap.
-// In the row-major ablation all 32 lanes also rebuild each layer's B operand
-// from the row-major weights into the slot's two B stages right before the
-// MMAs that read it.
-template <int V>
-__device__ __forceinline__ void run_slot_control(const FusedParams& p, const Ctx& c, int32_t s,
-                                                 int lane) {
+// ------------------------------------------------------------------ input producer
+// Lane 0 of the producer warp loads the input tiles of all slots in the order
+// the slots consume them (tile i goes to slot i % S, round i / S), each into
+// its slot's ring stage once the layer-1 MMAs of the round that used the
+// stage D rounds earlier have completed. Issuing a TMA load holds the issuing
+// thread for hundreds of cycles, so no control thread does it.
+__device__ __forceinline__ void run_input_producer(const FusedParams& p, const Ctx& c) {
   const int32_t S = static_cast<int32_t>(p.n_slots);
-  const uint32_t D = p.n_in_stages;  // input stages of this slot
-  const int L = p.L;
-  const int32_t n_rounds = (c.n_local - s + S - 1) / S;  // tiles r*S + s < n_local
-  int32_t issued = -1;  // last round whose input load was issued
+  const uint32_t D = p.n_in_stages;
+  const uint32_t tx = static_cast<uint32_t>(kTileM * 2 * p.d0);
+  for (int k = 0; k < 3; ++k) prefetch_tensormap(&p.tm_in[k]);
   bool ok = true;
-  if (lane == 0) {
-    if (p.test_stall) ok = wait_phase(c.bar(kBarNever), 0, p.wait_ns, c.abort_flag, p.status);
-    if (ok) ok = wait_phase(c.bar(kBarWLoad), 0, p.wait_ns, c.abort_flag, p.status);
+  int32_t i = 0;
+  for (; i < c.n_local && ok; ++i) {
+    const int32_t s = i % S;
+    const uint32_t r = static_cast<uint32_t>(i / S);
+    const uint32_t st = static_cast<uint32_t>(s) * D + r % D;
+    ok = wait_phase(c.bar(kBarInEmpty + st), ((r / D) & 1u) ^ 1u, p.wait_ns, c.abort_flag,
+                    p.status);
+    if (!ok) break;
+    mbar_arrive_expect_tx(c.bar(kBarInFull + st), tx);
+    issue_input_tma(p, c.sbase + p.sm_in + st * p.in_stage_bytes, c.bar(kBarInFull + st), tile_of(i));
   }
-  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-  uint32_t g = 0;  // B stages used (row-major ablation)
-  for (int32_t r = 0; r < n_rounds && ok; ++r) {
-    if (lane == 0) {
-      // Keep the input ring D rounds ahead. A stage is free once the layer-1
-      // MMAs of the round that used it D rounds ago have completed.
-      while (ok && issued + 1 < r + static_cast<int32_t>(D) && issued + 1 < n_rounds) {
-        const uint32_t rr = static_cast<uint32_t>(issued + 1);
-        const uint32_t st = static_cast<uint32_t>(s) * D + rr % D;
-        ok = wait_phase(c.bar(kBarInEmpty + st), ((rr / D) & 1u) ^ 1u, p.wait_ns, c.abort_flag,
-                        p.status);
-        if (!ok) break;
-        mbar_arrive_expect_tx(c.bar(kBarInFull + st), static_cast<uint32_t>(kTileM * 2 * p.d0));
-        issue_input_tma(p, c.sbase + p.sm_in + st * p.in_stage_bytes, c.bar(kBarInFull + st),
-                        tile_of(static_cast<int32_t>(rr) * S + s));
-        issued = static_cast<int32_t>(rr);
+  // Drain: the loads of the last D rounds of every slot (the latest fill of
+  // every stage) must land before the CTA may exit.
+  for (int32_t j = i - 1; j >= 0 && j >= i - S * static_cast<int32_t>(D); --j) {
+    const uint32_t r = static_cast<uint32_t>(j / S);
+    const uint32_t st = static_cast<uint32_t>(j % S) * D + r % D;
+    wait_drain(c.bar(kBarInFull + st), (r / D) & 1u, p.status);
+  }
+}
+
+// Output staging of one tile: a region per 32-column chunk of the output
+// (128 rows x 64 bytes, 64-byte swizzle; a trailing 16-column chunk gets
+// 128 x 32 bytes, 32-byte swizzle), each 1024-aligned. A warp stores the rows
+// of its lane quadrant of its own chunks with its own TMA stores, so no warp
+// ever waits for another.
+__device__ __forceinline__ uint32_t out_chunk_off(int c0) {
+  return static_cast<uint32_t>(c0 >> 5) * (kTileM * 64u);
+}
+
+// ------------------------------------------------------------------ resident weights
+// Tile slot s is served by its own 4G warps (4 TMEM lane quadrants x G column
+// groups). Per layer evaluation (chain) they wait for the accumulator, round
+// and activate it into the slot's A region in TMEM (or, after the last layer,
+// into the output staging tile), and meet at the slot's named barrier; then
+// one lane of theirs (the issuer) issues the next chain's tcgen05.mma
+// sequence and commits it to the slot's accumulator barrier. There is no
+// hand-off to another warp between a layer's epilogue and the next layer's
+// MMAs: a named barrier costs tens of cycles, an mbarrier hand-off between
+// warps a hundred or more. The four or five slots' issuers sit in different
+// warps, so their MMA issue latencies overlap.
+//
+// Every warp of a slot passes the same sequence of named barriers whatever
+// happens: a failed wait only turns the remaining work off (`ok`), so no warp
+// can be left waiting at a barrier that another has stepped past.
+//
+// In the row-major ablation the slot's warps also rebuild the next layer's B
+// operand from the row-major weights into the slot's B stage before they
+// meet (the chain that read the stage has completed by then).
+template <int V>
+__device__ __forceinline__ void run_slot_resident(const FusedParams& p, const Ctx& c, int warp,
+                                                  int lane) {
+  const int32_t S = static_cast<int32_t>(p.n_slots);
+  const int G = static_cast<int>(p.n_groups);
+  const int nw = 4 * G;  // warps of this slot
+  const int32_t s = warp / nw;
+  const int g = (warp % nw) / 4;
+  const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+  const int wi = warp % nw;   // index among the slot's warps
+  const bool issuer_warp = (g == 0) && (quad == (s & 3));
+  const bool issuer = issuer_warp && lane == 0;
+  const uint32_t row = static_cast<uint32_t>(quad * 32 + lane);
+  const uint32_t lane_bits = static_cast<uint32_t>(quad * 32) << 16;
+  const uint32_t slot_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
+  const uint32_t tbase = slot_tmem + lane_bits;
+  const uint32_t a_tmem = tbase + p.a_col;
+  const uint32_t bar_id = 1u + static_cast<uint32_t>(s);
+  const uint32_t bar_threads = 32u * static_cast<uint32_t>(nw);
+  const __half2 slope2 = __float2half2_rn(0.01f);  // half(0.01)
+  const int L = p.L;
+  const int n_out = p.dL;
+  const uint32_t D = p.n_in_stages;
+  const int32_t n_rounds = (c.n_local - s + S - 1) / S;  // tiles r*S + s < n_local
+  const bool storer = (lane == 0) && (32 * g < n_out);
+  const uint32_t b_stage = c.sbase + p.sm_b + static_cast<uint32_t>(s) * p.b_stage_bytes;
+
+  // Row-major ablation: this warp's share (rows wi, wi + nw, ...) of W_l
+  // rebuilt in the slot's B stage, 16-byte loads, swizzled 16-byte stores.
+  auto rebuild_b = [&](int l) {
+    const LayerRegs li = load_layer(p, c, l);
+    const int K = li.K, N = li.N, kc = K >> 3;
+    const uint16_t* Wl = p.mirror + li.rm_off;
+    for (int idx = wi * 32 + lane; idx < N * kc; idx += 32 * nw) {
+      const int n = idx / kc, col = (idx - n * kc) << 3;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(Wl + n * K + col));
+      uint32_t off;
+      int w, k0;
+      locate(static_cast<uint32_t>(N), K, col, off, w, k0);
+      st_shared_v4(b_stage + off + swz(static_cast<uint32_t>(n * 2 * w + (col - k0) * 2), w), v.x,
+                   v.y, v.z, v.w);
+    }
+    fence_proxy_async_smem();  // generic-proxy stores -> MMA reads (async proxy)
+  };
+
+  // The issuer: chain (round rr, layer l). Layer 1 reads the input tile in
+  // shared memory once it has landed; later layers read A from TMEM. The
+  // bias MMA (ones slab x bias slab) closes every chain.
+  auto issue = [&](int32_t rr, int l) -> bool {
+    const LayerRegs li = load_layer(p, c, l);
+    const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(rr) % D;
+    const uint32_t b_base = (V == kVarRowMajor) ? b_stage : c.sbase + p.sm_w + li.w_off;
+    const uint64_t b_add = b_base >> 4;
+    const uint32_t nslab = li.slab_end - li.slab_begin;
+    const uint32_t tab = c.slab_addr(p, li.slab_begin);
+    const uint64_t bias_bd = smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u);
+    bool ok = true;
+    if (l == 0) {
+      const uint64_t a_add = (c.sbase + p.sm_in + st * p.in_stage_bytes) >> 4;
+      auto wait = [&]() -> bool {
+        return wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(rr) / D) & 1u, p.wait_ns,
+                          c.abort_flag, p.status);
+      };
+      ok = mma_chain_ss(nslab, slot_tmem, tab, a_add, b_add, li.idesc, wait);
+    } else {
+      tc_fence_after_sync();
+      mma_chain_ts(nslab, slot_tmem, slot_tmem + p.a_col, tab, b_add, li.idesc);
+    }
+    if (ok) {
+      umma_f16_ts(slot_tmem, c.tmem + p.ones_col, bias_bd, li.idesc, 1u);
+      umma_commit(c.bar(kBarAccFull + s));
+      if (l == 0) umma_commit(c.bar(kBarInEmpty + st));
+    }
+    return ok;
+  };
+
+  bool ok = warp_wait(c.bar(kBarWLoad), 0, p, c);
+  if (issuer_warp) {
+    bool iok = ok;
+    if (issuer && iok && p.test_stall)
+      iok = wait_phase(c.bar(kBarNever), 0, p.wait_ns, c.abort_flag, p.status);
+    ok = __shfl_sync(0xFFFFFFFFu, iok, 0);
+  }
+  if (n_rounds > 0) {
+    if (V == kVarRowMajor && ok) rebuild_b(0);
+    named_bar_sync(bar_id, bar_threads);
+    if (issuer_warp) {
+      bool iok = ok;
+      if (iok && elect_one()) iok = issue(0, 0);
+      ok = __shfl_sync(0xFFFFFFFFu, iok, 0);
+    }
+  }
+  for (int32_t r = 0; r < n_rounds; ++r) {
+    const int32_t t = tile_of(r * S + s);
+    // Hidden layers: accumulator -> FP16 -> activation -> next layer's A.
+    for (int l = 0; l < L - 1; ++l) {
+      const uint32_t q = static_cast<uint32_t>(r * L + l);
+      const int N = load_layer(p, c, l).N;  // fetched before the wait
+      if (ok) ok = warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c);
+      if (ok) {
+        tc_fence_after_sync();
+        for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
+          uint32_t acc[32], h[16];
+          tmem_ld_x32(tbase + static_cast<uint32_t>(c0), acc);
+          tmem_wait_ld();
+          convert_pairs<V, 16, true>(acc, slope2, h);
+          tmem_st_x16(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
+        }
+        if ((N & 31) && ((N >> 5) % G) == g) {
+          const int c0 = N - 16;
+          uint32_t acc[16], h[8];
+          tmem_ld_x16(tbase + static_cast<uint32_t>(c0), acc);
+          tmem_wait_ld();
+          convert_pairs<V, 8, true>(acc, slope2, h);
+          tmem_st_x8(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
+        }
+        if (V == kVarRowMajor) rebuild_b(l + 1);
+        tmem_wait_st();
+      }
+      tc_fence_before_sync();
+      named_bar_sync(bar_id, bar_threads);
+      if (issuer_warp) {
+        bool iok = ok;
+        if (iok && elect_one()) iok = issue(r, l + 1);
+        ok = __shfl_sync(0xFFFFFFFFu, iok, 0);
       }
     }
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(r) % D;
-    for (int l = 0; l < L && ok; ++l) {
-      const LayerRegs li = load_layer(p, c, l);
-      uint32_t b_base = c.sbase + p.sm_w + li.w_off, bs = 0;
-      if (V == kVarRowMajor) {
-        // Rebuild W_l in one of this slot's two B stages from the row-major
-        // weights: 16-byte row-major loads, swizzled 16-byte smem stores.
-        bs = static_cast<uint32_t>(s) * 2u + (g & 1u);
-        ok = warp_wait(c.bar(kBarBEmpty + bs), ((g >> 1) & 1u) ^ 1u, p, c);
-        if (!ok) break;
-        b_base = c.sbase + p.sm_b + bs * p.b_stage_bytes;
-        const int K = li.K, N = li.N, kc = K >> 3;
-        const uint16_t* Wl = p.mirror + li.rm_off;
-        for (int idx = lane; idx < N * kc; idx += 32) {
-          const int n = idx / kc, col = (idx - n * kc) << 3;
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(Wl + n * K + col));
-          uint32_t off;
-          int w, k0;
-          locate(static_cast<uint32_t>(N), K, col, off, w, k0);
-          st_shared_v4(b_base + off + swz(static_cast<uint32_t>(n * 2 * w + (col - k0) * 2), w), v.x,
-                       v.y, v.z, v.w);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
+    // Last layer: accumulator -> FP16 -> output staging -> TMA store; the
+    // slot then starts its next tile.
+    {
+      const int l = L - 1;
+      const uint32_t q = static_cast<uint32_t>(r * L + l);
+      const int N = n_out;
+      const uint32_t out_dst =
+          c.sbase + p.sm_out +
+          (static_cast<uint32_t>(s) * p.n_out_bufs + static_cast<uint32_t>(r) % p.n_out_bufs) *
+              p.out_slot_bytes;
+      // This staging buffer went to this warp's TMA stores n_out_bufs tiles
+      // of this slot ago; they must have finished reading it (checked before
+      // the accumulator wait, which it does not depend on).
+      if (storer) {
+        if (p.n_out_bufs > 1)
+          bulk_wait_group_read<1>();
+        else
+          bulk_wait_group_read<0>();
       }
-      if (lane == 0) {
-        // Everything the MMA issue needs is computed before the wait, so that
-        // the MMAs follow the wake-up directly.
-        const uint64_t b_add = b_base >> 4;
-        const uint32_t slot_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
-        const uint32_t nslab = li.slab_end - li.slab_begin;
-        const uint32_t tab = c.slab_addr(p, li.slab_begin);
-        const uint64_t bias_bd = smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u);
-        const uint64_t a_add = (c.sbase + p.sm_in + st * p.in_stage_bytes) >> 4;
-        const int32_t q = r * L + l - 1;  // completion of this slot's previous epilogue
-        auto wait = [&]() -> bool {
-          bool w_ok = true;
-          if (q >= 0)
-            w_ok = spin_phase(c.bar(kBarActReady + s), static_cast<uint32_t>(q) & 1u, p.wait_ns,
-                              c.abort_flag, p.status);
-          if (w_ok && l == 0)
-            w_ok = wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(r) / D) & 1u,
-                              p.wait_ns, c.abort_flag, p.status);
-          return w_ok;
-        };
-        if (l == 0) {
-          // Layer 1: A is the input tile in shared memory.
-          ok = mma_chain_ss(nslab, slot_tmem, tab, a_add, b_add, li.idesc, wait);
-          // Bias: one more K=16 MMA, ones column x bias slab, added last.
-          if (ok)
-            umma_f16_ss(slot_tmem, smem_desc(c.sbase + p.sm_ones, 256u, 6u), bias_bd, li.idesc, 1u);
-        } else {
-          // Later layers: A is the previous epilogue's FP16 output in TMEM,
-          // 8 columns per 16-wide k-slab.
-          ok = mma_chain_ts(nslab, slot_tmem, slot_tmem + p.a_col, tab, b_add, li.idesc, wait);
-          if (ok) umma_f16_ts(slot_tmem, slot_tmem + p.a_ones, bias_bd, li.idesc, 1u);
+      __syncwarp();
+      if (ok) ok = warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c);
+      if (ok) {
+        tc_fence_after_sync();
+        for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
+          uint32_t acc[32], h[16];
+          tmem_ld_x32(tbase + static_cast<uint32_t>(c0), acc);
+          tmem_wait_ld();
+          convert_pairs<V, 16, false>(acc, slope2, h);
+          const uint32_t base = out_dst + out_chunk_off(c0);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            st_shared_v4_nc(base + swz(row * 64u + cc * 16u, 32), h[4 * cc], h[4 * cc + 1],
+                            h[4 * cc + 2], h[4 * cc + 3]);
         }
-        if (ok) {
-          umma_commit(c.bar(kBarAccFull + s));
-          if (l == 0) umma_commit(c.bar(kBarInEmpty + st));
-          if (V == kVarRowMajor) umma_commit(c.bar(kBarBEmpty + bs));
+        if ((N & 31) && ((N >> 5) % G) == g) {
+          const int c0 = N - 16;
+          uint32_t acc[16], h[8];
+          tmem_ld_x16(tbase + static_cast<uint32_t>(c0), acc);
+          tmem_wait_ld();
+          convert_pairs<V, 8, false>(acc, slope2, h);
+          const uint32_t base = out_dst + out_chunk_off(c0);
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc)
+            st_shared_v4_nc(base + swz(row * 32u + cc * 16u, 16), h[4 * cc], h[4 * cc + 1],
+                            h[4 * cc + 2], h[4 * cc + 3]);
+        }
+        if (V == kVarRowMajor && r + 1 < n_rounds) rebuild_b(0);
+        fence_proxy_async_smem();  // staging tile -> TMA store (async proxy)
+      }
+      tc_fence_before_sync();
+      named_bar_sync(bar_id, bar_threads);
+      if (issuer_warp) {
+        bool iok = ok;
+        if (iok && r + 1 < n_rounds && elect_one()) iok = issue(r + 1, 0);
+        ok = __shfl_sync(0xFFFFFFFFu, iok, 0);
+      }
+      if (storer && ok) {
+        const int64_t row0 = static_cast<int64_t>(t) * kTileM + quad * 32;
+        if (row0 < p.n) {
+          for (int c0 = 32 * g; c0 < N; c0 += 32 * G) {
+            const int cols = (N - c0 >= 32) ? 32 : 16;
+            tma_store_2d(&p.tm_out[swizzle_kind(cols)],
+                         out_dst + out_chunk_off(c0) + static_cast<uint32_t>(quad * 32 * 2 * cols),
+                         c0, static_cast<int32_t>(row0));
+          }
         }
       }
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      ++g;
+      if (storer) bulk_commit_group();
     }
   }
-  if (lane == 0) {
-    // Drain: every MMA this thread issued completes, and every input load it
-    // issued lands, before the CTA may exit.
+  if (issuer) {
+    // Drain: every MMA this thread issued completes before the CTA may exit.
     umma_commit(c.bar(kBarDrain + s));
     wait_drain(c.bar(kBarDrain + s), 0, p.status);
-    for (int32_t rr = (issued - static_cast<int32_t>(D) + 1 > 0 ? issued - static_cast<int32_t>(D) + 1 : 0);
-         rr <= issued; ++rr) {
-      const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(rr) % D;
-      wait_drain(c.bar(kBarInFull + st), (static_cast<uint32_t>(rr) / D) & 1u, p.status);
-    }
   }
+  if (storer) bulk_wait_group_all();
 }
 
 // ------------------------------------------------------------------ streamed weights
@@ -464,39 +625,32 @@ __device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, co
   const int L = p.L;
   const int32_t n_rounds_all = (c.n_local + S - 1) / S;   // rounds of the whole CTA
   const int32_t n_rounds = (c.n_local - s + S - 1) / S;   // rounds with a tile of this slot
-  int32_t issued = -1;
   bool ok = true;
   if (p.test_stall) ok = wait_phase(c.bar(kBarNever), 0, p.wait_ns, c.abort_flag, p.status);
   if (ok) ok = wait_phase(c.bar(kBarWLoad), 0, p.wait_ns, c.abort_flag, p.status);
   const uint32_t slot_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
+  const uint64_t ones_ad = smem_desc(c.sbase + p.sm_ones, 256u, 6u);
   // Weight ring position, kept incrementally (no division on the critical
   // path): the next stage to consume and the parity of its current fill.
   uint32_t ws = 0, wph = 0;
   for (int32_t r = 0; r < n_rounds_all && ok; ++r) {
     const bool has_tile = r < n_rounds;
-    while (ok && has_tile && issued + 1 < r + static_cast<int32_t>(D) && issued + 1 < n_rounds) {
-      const uint32_t rr = static_cast<uint32_t>(issued + 1);
-      const uint32_t st = static_cast<uint32_t>(s) * D + rr % D;
-      ok = wait_phase(c.bar(kBarInEmpty + st), ((rr / D) & 1u) ^ 1u, p.wait_ns, c.abort_flag,
-                      p.status);
-      if (!ok) break;
-      mbar_arrive_expect_tx(c.bar(kBarInFull + st), static_cast<uint32_t>(kTileM * 2 * p.d0));
-      issue_input_tma(p, c.sbase + p.sm_in + st * p.in_stage_bytes, c.bar(kBarInFull + st),
-                      tile_of(static_cast<int32_t>(rr) * S + s));
-      issued = static_cast<int32_t>(rr);
-    }
     const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(r) % D;
     const uint32_t in_base = c.sbase + p.sm_in + st * p.in_stage_bytes;
     for (int l = 0; l < L && ok; ++l) {
       const LayerRegs li = load_layer(p, c, l);
+      const uint32_t q = static_cast<uint32_t>(r * L + l);
+      const uint32_t d_tmem = slot_tmem + (q & 1u) * p.region_cols;
+      const uint32_t a_tmem = slot_tmem + ((q & 1u) ^ 1u) * p.region_cols;
       // The first K-segment's geometry, computed before the wait.
       uint32_t aoff;
       int w, k0;
       locate(kTileM, li.K, 0, aoff, w, k0);
       if (has_tile) {
-        const int32_t q = r * L + l - 1;
-        if (q >= 0)
-          ok = spin_phase(c.bar(kBarActReady + s), static_cast<uint32_t>(q) & 1u, p.wait_ns,
+        // Layer 1 needs the previous epilogue's first report (chain q - 1
+        // complete), later layers all of its columns.
+        if (q > 0)
+          ok = spin_phase(c.bar((l == 0 ? kBarHalf0 : kBarHalf1) + s), (q - 1u) & 1u, p.wait_ns,
                           c.abort_flag, p.status);
         if (ok && l == 0)
           ok = wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(r) / D) & 1u, p.wait_ns,
@@ -519,28 +673,31 @@ __device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, co
           if (l == 0) {
             const uint64_t ad = smem_desc(in_base + aoff, sbo, swc);
             if (w == 64) {
-              umma_f16_ss(slot_tmem, ad, bd, li.idesc, acc0);
-              umma_f16_ss(slot_tmem, ad + 2u, bd + 2u, li.idesc, 1u);
-              umma_f16_ss(slot_tmem, ad + 4u, bd + 4u, li.idesc, 1u);
-              umma_f16_ss(slot_tmem, ad + 6u, bd + 6u, li.idesc, 1u);
+              umma_f16_ss(d_tmem, ad, bd, li.idesc, acc0);
+              umma_f16_ss(d_tmem, ad + 2u, bd + 2u, li.idesc, 1u);
+              umma_f16_ss(d_tmem, ad + 4u, bd + 4u, li.idesc, 1u);
+              umma_f16_ss(d_tmem, ad + 6u, bd + 6u, li.idesc, 1u);
             } else if (w == 32) {
-              umma_f16_ss(slot_tmem, ad, bd, li.idesc, acc0);
-              umma_f16_ss(slot_tmem, ad + 2u, bd + 2u, li.idesc, 1u);
+              umma_f16_ss(d_tmem, ad, bd, li.idesc, acc0);
+              umma_f16_ss(d_tmem, ad + 2u, bd + 2u, li.idesc, 1u);
             } else {
-              umma_f16_ss(slot_tmem, ad, bd, li.idesc, acc0);
+              umma_f16_ss(d_tmem, ad, bd, li.idesc, acc0);
             }
           } else {
-            const uint32_t at = slot_tmem + p.a_col + static_cast<uint32_t>(k0 >> 1);
+            // Slab k0 / 16 is even (segments start at multiples of 16 that
+            // are 32-aligned except a trailing 16-wide one, which is then
+            // the only slab of its chunk).
+            const uint32_t at = a_tmem + a_slab_col(static_cast<uint32_t>(k0 >> 4));
             if (w == 64) {
-              umma_f16_ts(slot_tmem, at, bd, li.idesc, acc0);
-              umma_f16_ts(slot_tmem, at + 8u, bd + 2u, li.idesc, 1u);
-              umma_f16_ts(slot_tmem, at + 16u, bd + 4u, li.idesc, 1u);
-              umma_f16_ts(slot_tmem, at + 24u, bd + 6u, li.idesc, 1u);
+              umma_f16_ts(d_tmem, at, bd, li.idesc, acc0);
+              umma_f16_ts(d_tmem, at + a_slab_col(1), bd + 2u, li.idesc, 1u);
+              umma_f16_ts(d_tmem, at + a_slab_col(2), bd + 4u, li.idesc, 1u);
+              umma_f16_ts(d_tmem, at + a_slab_col(3), bd + 6u, li.idesc, 1u);
             } else if (w == 32) {
-              umma_f16_ts(slot_tmem, at, bd, li.idesc, acc0);
-              umma_f16_ts(slot_tmem, at + 8u, bd + 2u, li.idesc, 1u);
+              umma_f16_ts(d_tmem, at, bd, li.idesc, acc0);
+              umma_f16_ts(d_tmem, at + a_slab_col(1), bd + 2u, li.idesc, 1u);
             } else {
-              umma_f16_ts(slot_tmem, at, bd, li.idesc, acc0);
+              umma_f16_ts(d_tmem, at, bd, li.idesc, acc0);
             }
           }
           umma_commit(c.bar(kBarWEmpty + ws));
@@ -556,10 +713,7 @@ __device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, co
       if (ok && has_tile) {
         // Bias: one more K=16 MMA, ones column x bias slab, added last.
         const uint64_t bias_bd = smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u);
-        if (l == 0)
-          umma_f16_ss(slot_tmem, smem_desc(c.sbase + p.sm_ones, 256u, 6u), bias_bd, li.idesc, 1u);
-        else
-          umma_f16_ts(slot_tmem, slot_tmem + p.a_ones, bias_bd, li.idesc, 1u);
+        umma_f16_ss(d_tmem, ones_ad, bias_bd, li.idesc, 1u);
         umma_commit(c.bar(kBarAccFull + s));
         if (l == 0) umma_commit(c.bar(kBarInEmpty + st));
       }
@@ -567,28 +721,22 @@ __device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, co
   }
   umma_commit(c.bar(kBarDrain + s));
   wait_drain(c.bar(kBarDrain + s), 0, p.status);
-  const int32_t lo = issued - static_cast<int32_t>(D) + 1 > 0 ? issued - static_cast<int32_t>(D) + 1 : 0;
-  for (int32_t rr = lo; rr <= issued; ++rr) {
-    const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(rr) % D;
-    wait_drain(c.bar(kBarInFull + st), (static_cast<uint32_t>(rr) / D) & 1u, p.status);
-  }
 }
 
 // ------------------------------------------------------------------ epilogue
-// Output staging of one tile: a region per 32-column chunk of the output
-// (128 rows x 64 bytes, 64-byte swizzle; a trailing 16-column chunk gets
-// 128 x 32 bytes, 32-byte swizzle), each 1024-aligned. A warp stores the rows
-// of its lane quadrant of its own chunks with its own TMA stores, so no warp
-// ever waits for another.
-__device__ __forceinline__ uint32_t out_chunk_off(int c0) {
-  return static_cast<uint32_t>(c0 >> 5) * (kTileM * 64u);
-}
 
 // Epilogue warp e serves tile slot e / (4G), column group (e % 4G) / 4 and
 // TMEM lane quadrant (warp index % 4), where G = 16 / (4 * slots) column
 // groups share the columns of a layer in 32-column chunks g, g + G, ...; a
 // trailing 16-column chunk (N % 32 == 16) belongs to the group whose turn it
-// is.
+// is. A warp only ever overwrites columns of a chunk it has itself just read,
+// so the column groups never wait for one another.
+//
+// Per chain the slot's warps arrive twice, once per warp: on the first-half
+// barrier when they have written the A slabs of chunks [0, C / 2) (C chunks
+// in all), on the second-half barrier when every chunk is done. After the
+// last layer the first arrival comes as soon as the chain has completed, and
+// the second once the accumulator has been read.
 template <int V>
 __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c, int warp,
                                              int lane) {
@@ -606,44 +754,52 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
   const bool storer = (lane == 0) && (32 * g < n_out);
   if (!warp_wait(c.bar(kBarWLoad), 0, p, c)) return;
   const uint32_t tbase = c.tmem + lane_bits + static_cast<uint32_t>(s) * p.slot_cols;
-  if (g == 0) {
-    // The constant A slab of the bias MMA for layers read from TMEM: column 0
-    // of every row holds (1.0, 0) as an FP16 pair, columns 1..7 zeros.
-    const uint32_t ones[8] = {0x3C00u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    tmem_st_x8(tbase + p.a_ones, ones);
+  // All of this warp's TMEM writes are complete and ordered before the
+  // arrival that lets the MMAs read them.
+  auto report = [&](int bar) {
     tmem_wait_st();
-  }
-  const uint32_t a_tmem = tbase + p.a_col;
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.bar(bar + s));
+  };
   for (int32_t r = 0; r * S + s < c.n_local; ++r) {
     const int32_t t = tile_of(r * S + s);
     bool ok = true;
-    // Hidden layers: accumulator -> FP16 -> activation -> next layer's A (TMEM).
+    // Hidden layers: accumulator -> FP16 -> activation -> next layer's A,
+    // written over the chunk's own first columns.
     for (int l = 0; l < L - 1; ++l) {
       const uint32_t q = static_cast<uint32_t>(r * L + l);
       const int N = load_layer(p, c, l).N;  // fetched before the wait
+      const int C = (N + 31) >> 5, C0 = C >> 1;
+      const uint32_t reg = tbase + (q & 1u) * p.region_cols;
       if (!warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
-        uint32_t acc[32], h[16];
-        tmem_ld_x32(tbase + static_cast<uint32_t>(c0), acc);
-        tmem_wait_ld();
-        convert_pairs<V, 16, true>(acc, slope2, h);
-        tmem_st_x16(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
+      bool first_done = false;
+      for (int ch = g; ch < C; ch += G) {
+        if (!first_done && ch >= C0) {
+          report(kBarHalf0);
+          first_done = true;
+        }
+        const uint32_t col = reg + static_cast<uint32_t>(32 * ch);
+        if (32 * ch + 32 <= N) {
+          uint32_t acc[32], h[16];
+          tmem_ld_x32(col, acc);
+          tmem_wait_ld();
+          convert_pairs<V, 16, true>(acc, slope2, h);
+          tmem_st_x16(col, h);
+        } else {  // trailing 16-column chunk
+          uint32_t acc[16], h[8];
+          tmem_ld_x16(col, acc);
+          tmem_wait_ld();
+          convert_pairs<V, 8, true>(acc, slope2, h);
+          tmem_st_x8(col, h);
+        }
       }
-      if ((N & 31) && ((N >> 5) % G) == g) {
-        const int c0 = N - 16;
-        uint32_t acc[16], h[8];
-        tmem_ld_x16(tbase + static_cast<uint32_t>(c0), acc);
-        tmem_wait_ld();
-        convert_pairs<V, 8, true>(acc, slope2, h);
-        tmem_st_x8(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
-      }
-      tmem_wait_st();
-      tc_fence_before_sync();
-      mbar_arrive(c.bar(kBarActReady + s));
+      if (!first_done) report(kBarHalf0);
+      report(kBarHalf1);
     }
     if (!ok) break;
     // Last layer: accumulator -> FP16 -> output staging -> TMA store.
@@ -651,6 +807,7 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
       const int l = L - 1;
       const uint32_t q = static_cast<uint32_t>(r * L + l);
       const int N = n_out;
+      const uint32_t reg = tbase + (q & 1u) * p.region_cols;
       const uint32_t out_dst =
           c.sbase + p.sm_out +
           (static_cast<uint32_t>(s) * p.n_out_bufs + static_cast<uint32_t>(r) % p.n_out_bufs) *
@@ -667,9 +824,12 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
       __syncwarp();
       if (!warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c)) break;
       tc_fence_after_sync();
+      // The chain has completed: the next tile's layer 1 may start (it
+      // accumulates in the other region).
+      if (lane == 0) mbar_arrive(c.bar(kBarHalf0 + s));
       for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
         uint32_t acc[32], h[16];
-        tmem_ld_x32(tbase + static_cast<uint32_t>(c0), acc);
+        tmem_ld_x32(reg + static_cast<uint32_t>(c0), acc);
         tmem_wait_ld();
         convert_pairs<V, 16, false>(acc, slope2, h);
         const uint32_t base = out_dst + out_chunk_off(c0);
@@ -681,7 +841,7 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
       if ((N & 31) && ((N >> 5) % G) == g) {
         const int c0 = N - 16;
         uint32_t acc[16], h[8];
-        tmem_ld_x16(tbase + static_cast<uint32_t>(c0), acc);
+        tmem_ld_x16(reg + static_cast<uint32_t>(c0), acc);
         tmem_wait_ld();
         convert_pairs<V, 8, false>(acc, slope2, h);
         const uint32_t base = out_dst + out_chunk_off(c0);
@@ -692,8 +852,8 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
       }
       tc_fence_before_sync();
       fence_proxy_async_smem();  // staging tile -> TMA store (async proxy)
-      mbar_arrive(c.bar(kBarActReady + s));
       __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(kBarHalf1 + s));
       if (storer) {
         const int64_t row0 = static_cast<int64_t>(t) * kTileM + quad * 32;
         if (row0 < p.n) {
@@ -712,7 +872,7 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
 }
 
 template <int V>
-__global__ void __launch_bounds__(kFusedThreads, 1)
+__global__ void __launch_bounds__(is_stream(V) ? kFusedThreads : 32 * (kMaxSlotWarps + 1), 1)
     fused_mlp_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -730,14 +890,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    const uint32_t epi_per_slot = 32u * kEpiWarps / p.n_slots;
+    const uint32_t epi_per_slot = kEpiWarps / p.n_slots;  // streamed: one arrival per epilogue warp
     for (int s = 0; s < kMaxInStages; ++s) {
       mbar_init(c.bar(kBarInFull + s), 1);
       mbar_init(c.bar(kBarInEmpty + s), 1);
     }
     for (int s = 0; s < kMaxSlots; ++s) {
       mbar_init(c.bar(kBarAccFull + s), 1);
-      mbar_init(c.bar(kBarActReady + s), epi_per_slot);
+      mbar_init(c.bar(kBarHalf0 + s), epi_per_slot);
+      mbar_init(c.bar(kBarHalf1 + s), epi_per_slot);
       mbar_init(c.bar(kBarDrain + s), 1);
     }
     for (int s = 0; s < kMaxBStages; ++s) mbar_init(c.bar(kBarBEmpty + s), 1);
@@ -761,7 +922,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     // concatenated biases is row j - bias_row0[l] of layer l's slab.
     const uint16_t* gb = reinterpret_cast<const uint16_t*>(p.blob + p.bias_off);
     const uint32_t total_rows = kTileM + p.n_bias;
-    for (uint32_t idx = threadIdx.x; idx < 2u * total_rows; idx += kFusedThreads) {
+    for (uint32_t idx = threadIdx.x; idx < 2u * total_rows; idx += blockDim.x) {
       const uint32_t rr = idx >> 1, ch = idx & 1u;
       uint32_t base, row, v;
       if (rr < kTileM) {
@@ -784,6 +945,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   c.tmem = *tmem_slot;
+  if (!is_stream(V)) {
+    // The constant A slab of every bias MMA: column 0 of every TMEM lane
+    // holds (1.0, 0) as an FP16 pair, columns 1..7 zeros.
+    if (warp < 4) {
+      const uint32_t ones[8] = {0x3C00u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      tmem_st_x8(c.tmem + (static_cast<uint32_t>(warp * 32) << 16) + p.ones_col, ones);
+      tmem_wait_st();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+  }
 
   if (warp == 0 && lane == 0) {
     // Stage the schedule (and the packed weight images) once for the whole
@@ -797,8 +970,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       bulk_load(c.sbase + p.sm_w + off, p.blob + off, bytes, c.bar(kBarWLoad));
     }
   }
-  if (warp < kCtrlWarps) {
-    if (is_stream(V)) {
+  const int slot_warps = static_cast<int>(blockDim.x >> 5) - 1;  // the last warp produces inputs
+  if constexpr (is_stream(V)) {
+    if (warp < kCtrlWarps) {
       if (lane == 0) {
         if (warp < static_cast<int>(p.n_slots))
           run_slot_control_stream<V>(p, c, warp);
@@ -806,12 +980,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           run_weight_producer(p, c);
       }
       __syncwarp();
-    } else if (warp < static_cast<int>(p.n_slots)) {
-      run_slot_control<V>(p, c, warp, lane);
+    } else if (warp < slot_warps) {
+      run_epilogue<V>(p, c, warp, lane);
     }
-    if (warp == 0 && lane == 0) wait_drain(c.bar(kBarWLoad), 0, p.status);
   } else {
-    run_epilogue<V>(p, c, warp, lane);
+    if (warp < slot_warps) run_slot_resident<V>(p, c, warp, lane);
+  }
+  if (warp == slot_warps) {
+    if (lane == 0) {
+      run_input_producer(p, c);
+      wait_drain(c.bar(kBarWLoad), 0, p.status);
+    }
+    __syncwarp();
   }
 
   tc_fence_before_sync();
@@ -859,11 +1039,11 @@ uint32_t build_schedule(const int32_t* dims, int L, const uint32_t* w_off, const
 
 uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint32_t smem_optin) {
   const int L = p.L;
-  uint32_t nmax = 0, act_w = 16, bstage = 0, nb = 0;
+  uint32_t nmax = 0, hmax = 16, bstage = 0, nb = 0;
   for (int l = 0; l < L; ++l) {
     const uint32_t N = static_cast<uint32_t>(dims[l + 1]);
     nmax = N > nmax ? N : nmax;
-    if (l < L - 1 && N > act_w) act_w = N;
+    if (l < L - 1 && N > hmax) hmax = N;
     const uint32_t ib = image_bytes(N, dims[l]);
     bstage = ib > bstage ? ib : bstage;
     nb += N;
@@ -871,13 +1051,7 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
   p.n_bias = nb;
   p.d0 = dims[0];
   p.dL = dims[L];
-  // TMEM per slot: the accumulator (widest layer) then the A region (half the
-  // widest hidden layer, two FP16 values per column), each a multiple of 32.
-  const uint32_t acc_cols = (nmax + 31u) & ~31u;
-  const uint32_t a_cols = ((act_w / 2u) + 8u + 31u) & ~31u;  // + the 8-column ones slab
-  p.a_col = acc_cols;
-  p.a_ones = acc_cols + act_w / 2u;
-  p.slot_cols = acc_cols + a_cols;
+  const uint32_t acc_cols = (nmax + 31u) & ~31u;  // widest layer, a multiple of 32
   // output staging: 8 KB per 32-column chunk, 4 KB for a trailing 16-column one
   p.out_slot_bytes = static_cast<uint32_t>(p.dL >> 5) * (kTileM * 64u) +
                      ((p.dL & 31) ? kTileM * 32u : 0u);
@@ -892,18 +1066,32 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
   }
   wseg = align1024(wseg);
 
-  // Resident weights first (most tile slots, 4, 2, 1, as TMEM allows; two
-  // input stages per slot before one; two output buffers before one). If the
-  // weights do not fit (fused and scalar-activation variants), stream them
-  // with at most 2 slots (a control warp must stay free to produce) and the
-  // deepest weight ring (4 down to 2 stages) that fits.
+  // Resident weights first: the most tile slots TMEM allows (up to 5; per
+  // slot the accumulator and the A region, plus one shared 32-column block
+  // for the ones slab), two input stages per slot before one, two output
+  // buffers before one. If the weights do not fit (fused and
+  // scalar-activation variants), stream them with at most 2 slots (two
+  // accumulator regions each; a control warp must stay free to produce) and
+  // the deepest weight ring (4 down to 2 stages) that fits.
   for (int mode = 0; mode < 2; ++mode) {
     const bool streamed = mode == 1;
     if (streamed && variant == kVarRowMajor) break;
-    for (uint32_t slots = kMaxSlots; slots >= 1; slots >>= 1) {
-      if (slots * p.slot_cols > 512u) continue;
-      if (streamed && slots > 2) continue;
-      p.n_b_stages = (variant == kVarRowMajor) ? 2u * slots : 0u;
+    if (streamed) {
+      p.region_cols = acc_cols;
+      p.slot_cols = 2u * acc_cols;
+      p.a_col = p.ones_col = 0;
+    } else {
+      p.a_col = acc_cols;
+      p.slot_cols = acc_cols + (((hmax / 2u) + 31u) & ~31u);
+      p.region_cols = 0;
+    }
+    const uint32_t max_slots = streamed ? static_cast<uint32_t>(kStreamSlots) : static_cast<uint32_t>(kMaxSlots);
+    for (uint32_t slots = max_slots; slots >= 1; --slots) {
+      const uint32_t used = slots * p.slot_cols + (streamed ? 0u : 32u);
+      if (used > 512u) continue;
+      if (streamed && (kEpiWarps % (4 * slots))) continue;
+      const uint32_t groups = streamed ? kEpiWarps / (4u * slots) : (slots >= 3 ? 1u : 4u / slots);
+      p.n_b_stages = (variant == kVarRowMajor) ? slots : 0u;
       for (uint32_t wst = streamed ? kMaxWStages : 0u; wst >= (streamed ? 2u : 0u); --wst) {
         for (uint32_t depth = 2; depth >= 1; --depth) {
           for (uint32_t obufs = kOutBufs; obufs >= 1; --obufs) {
@@ -929,9 +1117,13 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
             const uint32_t total = off + 1024u;  // + alignment slack of the dynamic smem base
             if (total <= smem_optin) {
               uint32_t cols = 32;
-              while (cols < slots * p.slot_cols) cols <<= 1;
+              while (cols < used) cols <<= 1;
               p.tmem_cols = cols;
+              p.ones_col = streamed ? 0u : slots * p.slot_cols;
               p.n_slots = slots;
+              p.n_groups = groups;
+              p.n_threads = streamed ? static_cast<uint32_t>(kFusedThreads)
+                                     : 32u * (4u * slots * groups + 1u);
               p.in_stage_bytes = stage;
               p.n_in_stages = depth;
               p.n_out_bufs = obufs;
@@ -961,7 +1153,7 @@ static cudaError_t launch_variant(const FusedParams& p, int grid, uint32_t smem,
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  fused_mlp_kernel<V><<<grid, kFusedThreads, smem, stream>>>(p);
+  fused_mlp_kernel<V><<<grid, p.n_threads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

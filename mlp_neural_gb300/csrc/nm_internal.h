@@ -11,12 +11,21 @@
 
 namespace nm {
 
-constexpr int kMaxSlots = 4;       // 128-sample tiles in flight per CTA (upper bound)
+#ifndef NM_MAX_SLOTS
+#define NM_MAX_SLOTS 5
+#endif
+constexpr int kMaxSlots = NM_MAX_SLOTS;  // 128-sample tiles in flight per CTA (upper bound)
 constexpr int kMaxInStages = 2 * kMaxSlots;  // input TMA ring: up to 2 stages per slot
-constexpr int kMaxBStages = 2 * kMaxSlots;   // row-major ablation: 2 B stages per slot
-constexpr int kCtrlWarps = kMaxSlots;        // one control warp (MMA issue + input TMA) per slot
-constexpr int kEpiWarps = 16;      // epilogue warps: slots x 4 lane quadrants x column groups
-constexpr int kFusedThreads = 32 * (kCtrlWarps + kEpiWarps);
+constexpr int kMaxBStages = kMaxSlots;       // row-major ablation: one B stage per slot
+// Resident weights: each slot's warps (4 TMEM lane quadrants x column groups)
+// run its epilogue and issue its MMAs; then one input-producer warp.
+constexpr int kMaxSlotWarps = 4 * kMaxSlots > 16 ? 4 * kMaxSlots : 16;
+// Streamed weights: 4 control warps (slot MMA issue, weight copies), 16
+// epilogue warps, one input-producer warp.
+constexpr int kCtrlWarps = 4;
+constexpr int kEpiWarps = 16;
+constexpr int kStreamSlots = 2;    // tile slots at most with streamed weights
+constexpr int kFusedThreads = 32 * (kCtrlWarps + kEpiWarps + 1);  // launch maximum
 constexpr int kOutBufs = 2;        // output staging buffers per slot (TMA-store double buffer)
 constexpr int kMaxSlabs = kMaxLayers * (kMaxDim / 16);
 constexpr uint32_t kStatusTimeout = 1u;
@@ -39,8 +48,9 @@ enum BarIndex : int {
   kBarInFull = 0,
   kBarInEmpty = kBarInFull + kMaxInStages,
   kBarAccFull = kBarInEmpty + kMaxInStages,
-  kBarActReady = kBarAccFull + kMaxSlots,
-  kBarBEmpty = kBarActReady + kMaxSlots,
+  kBarHalf0 = kBarAccFull + kMaxSlots,   // epilogue: first half of the columns done
+  kBarHalf1 = kBarHalf0 + kMaxSlots,     // epilogue: all columns done
+  kBarBEmpty = kBarHalf1 + kMaxSlots,
   kBarWFull = kBarBEmpty + kMaxBStages,   // streamed-weight ring
   kBarWEmpty = kBarWFull + 4,
   kBarWLoad = kBarWEmpty + 4,
@@ -86,9 +96,9 @@ uint32_t build_schedule(const int32_t* dims, int L, const uint32_t* w_off, const
 
 // The bias enters through the tensor core: every layer's MMA chain ends with
 // one more K=16 MMA whose A slab is a "ones" column (A[r][0] = 1, the rest 0)
-// and whose B slab is the "bias slab" (B[n][0] = b[n], the rest 0), both in
-// the 32-byte-swizzle K-major layout. It adds b[n] to the FP32 accumulator
-// after the sum of products, as the arithmetic prescribes.
+// in shared memory and whose B slab is the "bias slab" (B[n][0] = b[n], the
+// rest 0), both in the 32-byte-swizzle K-major layout. It adds b[n] to the
+// FP32 accumulator after the sum of products, as the arithmetic prescribes.
 constexpr uint32_t kOnesTileBytes = 128u * 32u;
 
 struct FusedParams {  // 128-byte aligned through its CUtensorMap members
@@ -113,11 +123,17 @@ struct FusedParams {  // 128-byte aligned through its CUtensorMap members
   uint32_t in_stage_bytes, out_slot_bytes, b_stage_bytes;
   uint32_t n_in_stages;  // input stages per slot
   uint32_t n_b_stages, n_out_bufs;
-  uint32_t n_slots;     // tiles in flight (1, 2 or 4); kEpiWarps / (4 * n_slots) column groups
+  uint32_t n_slots;     // tiles in flight
+  uint32_t n_groups;    // column groups of a slot's epilogue (4 * n_groups warps per slot)
+  uint32_t n_threads;   // block size
   uint32_t tmem_cols;   // allocated TMEM columns (power of two)
-  uint32_t slot_cols;   // TMEM columns per tile slot: accumulator, then the A region
-  uint32_t a_col;       // column of the A region (next layer's FP16 activations) in a slot
-  uint32_t a_ones;      // column of the constant "ones" A slab (8 columns) in a slot
+  uint32_t slot_cols;   // TMEM columns per tile slot
+  // Resident weights: a slot holds its accumulator (columns [0, a_col)) and
+  // the next layer's FP16 A (from a_col); one "ones" slab (8 columns) at
+  // ones_col serves every slot's bias MMA.
+  uint32_t a_col, ones_col;
+  // Streamed weights: a slot holds two accumulator regions of region_cols.
+  uint32_t region_cols;
   uint32_t stream_w;    // 1: weights streamed through the ring instead of resident
   uint32_t n_wstages;   // streamed-weight ring depth
   uint32_t wstage_bytes;
