@@ -11,10 +11,7 @@
 
 namespace nm {
 
-#ifndef NM_MAX_SLOTS
-#define NM_MAX_SLOTS 5
-#endif
-constexpr int kMaxSlots = NM_MAX_SLOTS;  // 128-sample tiles in flight per CTA (upper bound)
+constexpr int kMaxSlots = 5;       // 128-sample tiles in flight per CTA (upper bound)
 constexpr int kMaxInStages = 2 * kMaxSlots;  // input TMA ring: up to 2 stages per slot
 constexpr int kMaxBStages = kMaxSlots;       // row-major ablation: one B stage per slot
 // Resident weights: each slot's warps (4 TMEM lane quadrants x column groups)
