@@ -134,32 +134,6 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, uint64
   return wait_phase_slow(bar, parity, limit_ns, abort_flag, status);
 }
 
-// Bounded wait by busy polling with test_wait: no suspend/wake-up latency.
-// Used by the single issuing thread of a control warp, where reacting fast
-// to the epilogue's arrival is on the critical path.
-__device__ __noinline__ bool spin_phase_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                             volatile uint32_t* abort_flag, uint32_t* status) {
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t spins = 0;
-  while (true) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if ((++spins & 255u) == 0u) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > limit_ns) {
-        *abort_flag = 1u;
-        atomicOr(status, kStatusTimeout);
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ bool spin_phase(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                           volatile uint32_t* abort_flag, uint32_t* status) {
-  if (mbar_test_wait(bar, parity)) return true;
-  return spin_phase_slow(bar, parity, limit_ns, abort_flag, status);
-}
-
 // Wait used while draining: ignores the abort flag, fixed limit.
 __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, uint32_t* status) {
   const uint64_t t0 = globaltimer_ns();
@@ -618,7 +592,7 @@ __device__ __forceinline__ void run_weight_producer(const FusedParams& p, const 
 
 template <int V>
 __device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, const Ctx& c,
-                                                        int32_t s) {
+                                                        int32_t s, int lane) {
   const int32_t S = static_cast<int32_t>(p.n_slots);
   const uint32_t D = p.n_in_stages;
   const uint32_t RW = p.n_wstages;
@@ -626,8 +600,8 @@ __device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, co
   const int32_t n_rounds_all = (c.n_local + S - 1) / S;   // rounds of the whole CTA
   const int32_t n_rounds = (c.n_local - s + S - 1) / S;   // rounds with a tile of this slot
   bool ok = true;
-  if (p.test_stall) ok = wait_phase(c.bar(kBarNever), 0, p.wait_ns, c.abort_flag, p.status);
-  if (ok) ok = wait_phase(c.bar(kBarWLoad), 0, p.wait_ns, c.abort_flag, p.status);
+  if (p.test_stall) ok = warp_wait(c.bar(kBarNever), 0, p, c);
+  if (ok) ok = warp_wait(c.bar(kBarWLoad), 0, p, c);
   const uint32_t slot_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
   const uint64_t ones_ad = smem_desc(c.sbase + p.sm_ones, 256u, 6u);
   // Weight ring position, kept incrementally (no division on the critical
@@ -649,19 +623,17 @@ __device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, co
       if (has_tile) {
         // Layer 1 needs the previous epilogue's first report (chain q - 1
         // complete), later layers all of its columns.
-        if (q > 0)
-          ok = spin_phase(c.bar((l == 0 ? kBarHalf0 : kBarHalf1) + s), (q - 1u) & 1u, p.wait_ns,
-                          c.abort_flag, p.status);
+        if (q > 0) ok = warp_wait(c.bar((l == 0 ? kBarHalf0 : kBarHalf1) + s), (q - 1u) & 1u, p, c);
         if (ok && l == 0)
-          ok = wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(r) / D) & 1u, p.wait_ns,
-                          c.abort_flag, p.status);
+          ok = warp_wait(c.bar(kBarInFull + st), (static_cast<uint32_t>(r) / D) & 1u, p, c);
       }
       for (int k = 0; k < li.K && ok;) {
         if (k > 0) locate(kTileM, li.K, k, aoff, w, k0);
-        ok = wait_phase(c.bar(kBarWFull + ws), wph, p.wait_ns, c.abort_flag, p.status);
+        ok = warp_wait(c.bar(kBarWFull + ws), wph, p, c);
         if (!ok) break;
         if (has_tile) {
           tc_fence_after_sync();
+          if (elect_one()) {
           // One K-segment: w / 16 k-slabs, 32 bytes apart in the segment's
           // swizzle atom, so slab j's descriptors are the segment's plus 2j
           // (start addresses are in 16-byte units). Issued straight-line.
@@ -701,8 +673,11 @@ __device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, co
             }
           }
           umma_commit(c.bar(kBarWEmpty + ws));
+          }
+          __syncwarp();
         } else {
-          mbar_arrive(c.bar(kBarWEmpty + ws));
+          if (lane == 0) mbar_arrive(c.bar(kBarWEmpty + ws));
+          __syncwarp();
         }
         if (++ws == RW) {
           ws = 0;
@@ -713,14 +688,20 @@ __device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, co
       if (ok && has_tile) {
         // Bias: one more K=16 MMA, ones column x bias slab, added last.
         const uint64_t bias_bd = smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u);
-        umma_f16_ss(d_tmem, ones_ad, bias_bd, li.idesc, 1u);
-        umma_commit(c.bar(kBarAccFull + s));
-        if (l == 0) umma_commit(c.bar(kBarInEmpty + st));
+        if (elect_one()) {
+          umma_f16_ss(d_tmem, ones_ad, bias_bd, li.idesc, 1u);
+          umma_commit(c.bar(kBarAccFull + s));
+          if (l == 0) umma_commit(c.bar(kBarInEmpty + st));
+        }
+        __syncwarp();
       }
     }
   }
-  umma_commit(c.bar(kBarDrain + s));
-  wait_drain(c.bar(kBarDrain + s), 0, p.status);
+  // Drain: every MMA this warp issued completes before the CTA may exit.
+  if (elect_one()) umma_commit(c.bar(kBarDrain + s));
+  __syncwarp();
+  if (lane == 0) wait_drain(c.bar(kBarDrain + s), 0, p.status);
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ epilogue
@@ -973,11 +954,10 @@ __global__ void __launch_bounds__(is_stream(V) ? kFusedThreads : 32 * (kMaxSlotW
   const int slot_warps = static_cast<int>(blockDim.x >> 5) - 1;  // the last warp produces inputs
   if constexpr (is_stream(V)) {
     if (warp < kCtrlWarps) {
-      if (lane == 0) {
-        if (warp < static_cast<int>(p.n_slots))
-          run_slot_control_stream<V>(p, c, warp);
-        else if (warp == static_cast<int>(p.n_slots))
-          run_weight_producer(p, c);
+      if (warp < static_cast<int>(p.n_slots)) {
+        run_slot_control_stream<V>(p, c, warp, lane);
+      } else if (warp == static_cast<int>(p.n_slots) && lane == 0) {
+        run_weight_producer(p, c);
       }
       __syncwarp();
     } else if (warp < slot_warps) {
