@@ -214,11 +214,6 @@ __device__ __forceinline__ bool mma_seq_ss(uint32_t d, uint32_t tab, uint64_t a_
   return true;
 }
 
-// Column of k-slab k of a layer's A operand inside the previous chain's
-// region (streamed-weight layout): the epilogue writes the 16 FP16 pairs of
-// accumulator chunk c (columns [32c, 32c + 32)) into the chunk's own first
-// 16 columns, slab 2c first, so slab k starts at 32 (k >> 1) + 8 (k & 1).
-__host__ __device__ constexpr uint32_t a_slab_col(uint32_t k) { return 32u * (k >> 1) + 8u * (k & 1u); }
 
 // Same with A in TMEM (resident-weight layout: k-slab k of the activations
 // starts 8 columns, 16 FP16 values per row, after slab k - 1); only the B
@@ -345,7 +340,7 @@ __device__ __forceinline__ uint32_t out_chunk_off(int c0) {
 // operand from the row-major weights into the slot's B stage before they
 // meet (the chain that read the stage has completed by then).
 template <int V>
-__device__ __forceinline__ void run_slot_resident(const FusedParams& p, const Ctx& c, int warp,
+__device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int warp,
                                                   int lane) {
   const int32_t S = static_cast<int32_t>(p.n_slots);
   const int G = static_cast<int>(p.n_groups);
@@ -392,7 +387,72 @@ __device__ __forceinline__ void run_slot_resident(const FusedParams& p, const Ct
   // The issuer: chain (round rr, layer l). Layer 1 reads the input tile in
   // shared memory once it has landed; later layers read A from TMEM. The
   // bias MMA (ones slab x bias slab) closes every chain.
+  // Streamed weights: the next weight-ring stage to consume and the parity
+  // of its current fill (kept by the issuing lane only).
+  uint32_t ws = 0, wph = 0;
+  auto next_stage = [&]() {
+    if (++ws == p.n_wstages) {
+      ws = 0;
+      wph ^= 1u;
+    }
+  };
+  // Streamed weights: the layer's K-segments are taken from the ring as the
+  // weight-producer warp fills it, in the (round, layer, segment) order in
+  // which every slot consumes it; each stage is released by a commit once
+  // this slot's MMAs on it complete.
+  auto issue_stream = [&](int32_t rr, int l) -> bool {
+    const LayerRegs li = load_layer(p, c, l);
+    const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(rr) % D;
+    const uint32_t in_base = c.sbase + p.sm_in + st * p.in_stage_bytes;
+    bool ok = true;
+    if (l == 0)
+      ok = wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(rr) / D) & 1u, p.wait_ns,
+                      c.abort_flag, p.status);
+    for (int k = 0; k < li.K && ok;) {
+      uint32_t aoff;
+      int w, k0;
+      locate(kTileM, li.K, k, aoff, w, k0);
+      ok = wait_phase(c.bar(kBarWFull + ws), wph, p.wait_ns, c.abort_flag, p.status);
+      if (!ok) break;
+      tc_fence_after_sync();
+      // One K-segment: w / 16 k-slabs, 32 bytes apart in the segment's
+      // swizzle atom, so slab j's descriptors are the segment's plus 2j
+      // (start addresses are in 16-byte units). Issued straight-line.
+      const uint32_t sbo = 16u * static_cast<uint32_t>(w);
+      const uint32_t swc = swizzle_code(w);
+      const uint64_t bd = smem_desc(c.sbase + p.sm_wring + ws * p.wstage_bytes, sbo, swc);
+      const uint32_t acc0 = static_cast<uint32_t>(k0);  // the layer's first slab overwrites
+      if (l == 0) {
+        const uint64_t ad = smem_desc(in_base + aoff, sbo, swc);
+        umma_f16_ss(slot_tmem, ad, bd, li.idesc, acc0);
+        if (w >= 32) umma_f16_ss(slot_tmem, ad + 2u, bd + 2u, li.idesc, 1u);
+        if (w == 64) {
+          umma_f16_ss(slot_tmem, ad + 4u, bd + 4u, li.idesc, 1u);
+          umma_f16_ss(slot_tmem, ad + 6u, bd + 6u, li.idesc, 1u);
+        }
+      } else {
+        const uint32_t at = slot_tmem + p.a_col + (static_cast<uint32_t>(k0) >> 1);
+        umma_f16_ts(slot_tmem, at, bd, li.idesc, acc0);
+        if (w >= 32) umma_f16_ts(slot_tmem, at + 8u, bd + 2u, li.idesc, 1u);
+        if (w == 64) {
+          umma_f16_ts(slot_tmem, at + 16u, bd + 4u, li.idesc, 1u);
+          umma_f16_ts(slot_tmem, at + 24u, bd + 6u, li.idesc, 1u);
+        }
+      }
+      umma_commit(c.bar(kBarWEmpty + ws));
+      next_stage();
+      k = k0 + w;
+    }
+    if (ok) {
+      umma_f16_ts(slot_tmem, c.tmem + p.ones_col,
+                  smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u), li.idesc, 1u);
+      umma_commit(c.bar(kBarAccFull + s));
+      if (l == 0) umma_commit(c.bar(kBarInEmpty + st));
+    }
+    return ok;
+  };
   auto issue = [&](int32_t rr, int l) -> bool {
+    if constexpr (is_stream(V)) return issue_stream(rr, l);
     const LayerRegs li = load_layer(p, c, l);
     const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(rr) % D;
     const uint32_t b_base = (V == kVarRowMajor) ? b_stage : c.sbase + p.sm_w + li.w_off;
@@ -541,6 +601,29 @@ __device__ __forceinline__ void run_slot_resident(const FusedParams& p, const Ct
       if (storer) bulk_commit_group();
     }
   }
+  if constexpr (is_stream(V)) {
+    // Rounds in which this slot has no tile: its share of releasing every
+    // weight-ring stage, without MMAs.
+    if (issuer_warp && ok && elect_one()) {
+      const int32_t n_rounds_all = (c.n_local + S - 1) / S;
+      bool wok = true;
+      for (int32_t r = n_rounds; r < n_rounds_all && wok; ++r) {
+        for (int l = 0; l < L && wok; ++l) {
+          const LayerRegs li = load_layer(p, c, l);
+          for (int k = 0; k < li.K && wok;) {
+            uint32_t off;
+            int w, k0;
+            locate(kTileM, li.K, k, off, w, k0);
+            wok = wait_phase(c.bar(kBarWFull + ws), wph, p.wait_ns, c.abort_flag, p.status);
+            if (wok) mbar_arrive(c.bar(kBarWEmpty + ws));
+            next_stage();
+            k = k0 + w;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  }
   if (issuer) {
     // Drain: every MMA this thread issued completes before the CTA may exit.
     umma_commit(c.bar(kBarDrain + s));
@@ -591,269 +674,7 @@ __device__ __forceinline__ void run_weight_producer(const FusedParams& p, const 
 }
 
 template <int V>
-__device__ __forceinline__ void run_slot_control_stream(const FusedParams& p, const Ctx& c,
-                                                        int32_t s, int lane) {
-  const int32_t S = static_cast<int32_t>(p.n_slots);
-  const uint32_t D = p.n_in_stages;
-  const uint32_t RW = p.n_wstages;
-  const int L = p.L;
-  const int32_t n_rounds_all = (c.n_local + S - 1) / S;   // rounds of the whole CTA
-  const int32_t n_rounds = (c.n_local - s + S - 1) / S;   // rounds with a tile of this slot
-  bool ok = true;
-  if (p.test_stall) ok = warp_wait(c.bar(kBarNever), 0, p, c);
-  if (ok) ok = warp_wait(c.bar(kBarWLoad), 0, p, c);
-  const uint32_t slot_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
-  const uint64_t ones_ad = smem_desc(c.sbase + p.sm_ones, 256u, 6u);
-  // Weight ring position, kept incrementally (no division on the critical
-  // path): the next stage to consume and the parity of its current fill.
-  uint32_t ws = 0, wph = 0;
-  for (int32_t r = 0; r < n_rounds_all && ok; ++r) {
-    const bool has_tile = r < n_rounds;
-    const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(r) % D;
-    const uint32_t in_base = c.sbase + p.sm_in + st * p.in_stage_bytes;
-    for (int l = 0; l < L && ok; ++l) {
-      const LayerRegs li = load_layer(p, c, l);
-      const uint32_t q = static_cast<uint32_t>(r * L + l);
-      const uint32_t d_tmem = slot_tmem + (q & 1u) * p.region_cols;
-      const uint32_t a_tmem = slot_tmem + ((q & 1u) ^ 1u) * p.region_cols;
-      // The first K-segment's geometry, computed before the wait.
-      uint32_t aoff;
-      int w, k0;
-      locate(kTileM, li.K, 0, aoff, w, k0);
-      if (has_tile) {
-        // Layer 1 needs the previous epilogue's first report (chain q - 1
-        // complete), later layers all of its columns.
-        if (q > 0) ok = warp_wait(c.bar((l == 0 ? kBarHalf0 : kBarHalf1) + s), (q - 1u) & 1u, p, c);
-        if (ok && l == 0)
-          ok = warp_wait(c.bar(kBarInFull + st), (static_cast<uint32_t>(r) / D) & 1u, p, c);
-      }
-      for (int k = 0; k < li.K && ok;) {
-        if (k > 0) locate(kTileM, li.K, k, aoff, w, k0);
-        ok = warp_wait(c.bar(kBarWFull + ws), wph, p, c);
-        if (!ok) break;
-        if (has_tile) {
-          tc_fence_after_sync();
-          if (elect_one()) {
-          // One K-segment: w / 16 k-slabs, 32 bytes apart in the segment's
-          // swizzle atom, so slab j's descriptors are the segment's plus 2j
-          // (start addresses are in 16-byte units). Issued straight-line.
-          const uint32_t stage = c.sbase + p.sm_wring + ws * p.wstage_bytes;
-          const uint32_t sbo = 16u * static_cast<uint32_t>(w);
-          const uint32_t swc = swizzle_code(w);
-          const uint64_t bd = smem_desc(stage, sbo, swc);
-          const uint32_t acc0 = static_cast<uint32_t>(k0);  // first slab of the layer overwrites
-          if (l == 0) {
-            const uint64_t ad = smem_desc(in_base + aoff, sbo, swc);
-            if (w == 64) {
-              umma_f16_ss(d_tmem, ad, bd, li.idesc, acc0);
-              umma_f16_ss(d_tmem, ad + 2u, bd + 2u, li.idesc, 1u);
-              umma_f16_ss(d_tmem, ad + 4u, bd + 4u, li.idesc, 1u);
-              umma_f16_ss(d_tmem, ad + 6u, bd + 6u, li.idesc, 1u);
-            } else if (w == 32) {
-              umma_f16_ss(d_tmem, ad, bd, li.idesc, acc0);
-              umma_f16_ss(d_tmem, ad + 2u, bd + 2u, li.idesc, 1u);
-            } else {
-              umma_f16_ss(d_tmem, ad, bd, li.idesc, acc0);
-            }
-          } else {
-            // Slab k0 / 16 is even (segments start at multiples of 16 that
-            // are 32-aligned except a trailing 16-wide one, which is then
-            // the only slab of its chunk).
-            const uint32_t at = a_tmem + a_slab_col(static_cast<uint32_t>(k0 >> 4));
-            if (w == 64) {
-              umma_f16_ts(d_tmem, at, bd, li.idesc, acc0);
-              umma_f16_ts(d_tmem, at + a_slab_col(1), bd + 2u, li.idesc, 1u);
-              umma_f16_ts(d_tmem, at + a_slab_col(2), bd + 4u, li.idesc, 1u);
-              umma_f16_ts(d_tmem, at + a_slab_col(3), bd + 6u, li.idesc, 1u);
-            } else if (w == 32) {
-              umma_f16_ts(d_tmem, at, bd, li.idesc, acc0);
-              umma_f16_ts(d_tmem, at + a_slab_col(1), bd + 2u, li.idesc, 1u);
-            } else {
-              umma_f16_ts(d_tmem, at, bd, li.idesc, acc0);
-            }
-          }
-          umma_commit(c.bar(kBarWEmpty + ws));
-          }
-          __syncwarp();
-        } else {
-          if (lane == 0) mbar_arrive(c.bar(kBarWEmpty + ws));
-          __syncwarp();
-        }
-        if (++ws == RW) {
-          ws = 0;
-          wph ^= 1u;
-        }
-        k = k0 + w;
-      }
-      if (ok && has_tile) {
-        // Bias: one more K=16 MMA, ones column x bias slab, added last.
-        const uint64_t bias_bd = smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u);
-        if (elect_one()) {
-          umma_f16_ss(d_tmem, ones_ad, bias_bd, li.idesc, 1u);
-          umma_commit(c.bar(kBarAccFull + s));
-          if (l == 0) umma_commit(c.bar(kBarInEmpty + st));
-        }
-        __syncwarp();
-      }
-    }
-  }
-  // Drain: every MMA this warp issued completes before the CTA may exit.
-  if (elect_one()) umma_commit(c.bar(kBarDrain + s));
-  __syncwarp();
-  if (lane == 0) wait_drain(c.bar(kBarDrain + s), 0, p.status);
-  __syncwarp();
-}
-
-// ------------------------------------------------------------------ epilogue
-
-// Epilogue warp e serves tile slot e / (4G), column group (e % 4G) / 4 and
-// TMEM lane quadrant (warp index % 4), where G = 16 / (4 * slots) column
-// groups share the columns of a layer in 32-column chunks g, g + G, ...; a
-// trailing 16-column chunk (N % 32 == 16) belongs to the group whose turn it
-// is. A warp only ever overwrites columns of a chunk it has itself just read,
-// so the column groups never wait for one another.
-//
-// Per chain the slot's warps arrive twice, once per warp: on the first-half
-// barrier when they have written the A slabs of chunks [0, C / 2) (C chunks
-// in all), on the second-half barrier when every chunk is done. After the
-// last layer the first arrival comes as soon as the chain has completed, and
-// the second once the accumulator has been read.
-template <int V>
-__device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c, int warp,
-                                             int lane) {
-  const int32_t S = static_cast<int32_t>(p.n_slots);
-  const int G = kEpiWarps / (4 * S);
-  const int e = warp - kCtrlWarps;
-  const int32_t s = e / (4 * G);
-  const int g = (e % (4 * G)) / 4;
-  const int quad = warp & 3;  // TMEM lane quadrant this warp may access
-  const uint32_t row = static_cast<uint32_t>(quad * 32 + lane);
-  const uint32_t lane_bits = static_cast<uint32_t>(quad * 32) << 16;
-  const __half2 slope2 = __float2half2_rn(0.01f);  // half(0.01)
-  const int L = p.L;
-  const int n_out = p.dL;
-  const bool storer = (lane == 0) && (32 * g < n_out);
-  if (!warp_wait(c.bar(kBarWLoad), 0, p, c)) return;
-  const uint32_t tbase = c.tmem + lane_bits + static_cast<uint32_t>(s) * p.slot_cols;
-  // All of this warp's TMEM writes are complete and ordered before the
-  // arrival that lets the MMAs read them.
-  auto report = [&](int bar) {
-    tmem_wait_st();
-    tc_fence_before_sync();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(c.bar(bar + s));
-  };
-  for (int32_t r = 0; r * S + s < c.n_local; ++r) {
-    const int32_t t = tile_of(r * S + s);
-    bool ok = true;
-    // Hidden layers: accumulator -> FP16 -> activation -> next layer's A,
-    // written over the chunk's own first columns.
-    for (int l = 0; l < L - 1; ++l) {
-      const uint32_t q = static_cast<uint32_t>(r * L + l);
-      const int N = load_layer(p, c, l).N;  // fetched before the wait
-      const int C = (N + 31) >> 5, C0 = C >> 1;
-      const uint32_t reg = tbase + (q & 1u) * p.region_cols;
-      if (!warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      bool first_done = false;
-      for (int ch = g; ch < C; ch += G) {
-        if (!first_done && ch >= C0) {
-          report(kBarHalf0);
-          first_done = true;
-        }
-        const uint32_t col = reg + static_cast<uint32_t>(32 * ch);
-        if (32 * ch + 32 <= N) {
-          uint32_t acc[32], h[16];
-          tmem_ld_x32(col, acc);
-          tmem_wait_ld();
-          convert_pairs<V, 16, true>(acc, slope2, h);
-          tmem_st_x16(col, h);
-        } else {  // trailing 16-column chunk
-          uint32_t acc[16], h[8];
-          tmem_ld_x16(col, acc);
-          tmem_wait_ld();
-          convert_pairs<V, 8, true>(acc, slope2, h);
-          tmem_st_x8(col, h);
-        }
-      }
-      if (!first_done) report(kBarHalf0);
-      report(kBarHalf1);
-    }
-    if (!ok) break;
-    // Last layer: accumulator -> FP16 -> output staging -> TMA store.
-    {
-      const int l = L - 1;
-      const uint32_t q = static_cast<uint32_t>(r * L + l);
-      const int N = n_out;
-      const uint32_t reg = tbase + (q & 1u) * p.region_cols;
-      const uint32_t out_dst =
-          c.sbase + p.sm_out +
-          (static_cast<uint32_t>(s) * p.n_out_bufs + static_cast<uint32_t>(r) % p.n_out_bufs) *
-              p.out_slot_bytes;
-      // This staging buffer went to this warp's TMA stores n_out_bufs tiles
-      // of this slot ago; they must have finished reading it (checked before
-      // the accumulator wait, which it does not depend on).
-      if (storer) {
-        if (p.n_out_bufs > 1)
-          bulk_wait_group_read<1>();
-        else
-          bulk_wait_group_read<0>();
-      }
-      __syncwarp();
-      if (!warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c)) break;
-      tc_fence_after_sync();
-      // The chain has completed: the next tile's layer 1 may start (it
-      // accumulates in the other region).
-      if (lane == 0) mbar_arrive(c.bar(kBarHalf0 + s));
-      for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
-        uint32_t acc[32], h[16];
-        tmem_ld_x32(reg + static_cast<uint32_t>(c0), acc);
-        tmem_wait_ld();
-        convert_pairs<V, 16, false>(acc, slope2, h);
-        const uint32_t base = out_dst + out_chunk_off(c0);
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-          st_shared_v4_nc(base + swz(row * 64u + cc * 16u, 32), h[4 * cc], h[4 * cc + 1],
-                          h[4 * cc + 2], h[4 * cc + 3]);
-      }
-      if ((N & 31) && ((N >> 5) % G) == g) {
-        const int c0 = N - 16;
-        uint32_t acc[16], h[8];
-        tmem_ld_x16(reg + static_cast<uint32_t>(c0), acc);
-        tmem_wait_ld();
-        convert_pairs<V, 8, false>(acc, slope2, h);
-        const uint32_t base = out_dst + out_chunk_off(c0);
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc)
-          st_shared_v4_nc(base + swz(row * 32u + cc * 16u, 16), h[4 * cc], h[4 * cc + 1],
-                          h[4 * cc + 2], h[4 * cc + 3]);
-      }
-      tc_fence_before_sync();
-      fence_proxy_async_smem();  // staging tile -> TMA store (async proxy)
-      __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(kBarHalf1 + s));
-      if (storer) {
-        const int64_t row0 = static_cast<int64_t>(t) * kTileM + quad * 32;
-        if (row0 < p.n) {
-          for (int c0 = 32 * g; c0 < N; c0 += 32 * G) {
-            const int cols = (N - c0 >= 32) ? 32 : 16;
-            tma_store_2d(&p.tm_out[swizzle_kind(cols)],
-                         out_dst + out_chunk_off(c0) + static_cast<uint32_t>(quad * 32 * 2 * cols),
-                         c0, static_cast<int32_t>(row0));
-          }
-        }
-        bulk_commit_group();
-      }
-    }
-  }
-  if (storer) bulk_wait_group_all();
-}
-
-template <int V>
-__global__ void __launch_bounds__(is_stream(V) ? kFusedThreads : 32 * (kMaxSlotWarps + 1), 1)
+__global__ void __launch_bounds__(is_stream(V) ? 32 * (16 + 2) : 32 * (kMaxSlotWarps + 1), 1)
     fused_mlp_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -871,15 +692,12 @@ __global__ void __launch_bounds__(is_stream(V) ? kFusedThreads : 32 * (kMaxSlotW
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    const uint32_t epi_per_slot = kEpiWarps / p.n_slots;  // streamed: one arrival per epilogue warp
     for (int s = 0; s < kMaxInStages; ++s) {
       mbar_init(c.bar(kBarInFull + s), 1);
       mbar_init(c.bar(kBarInEmpty + s), 1);
     }
     for (int s = 0; s < kMaxSlots; ++s) {
       mbar_init(c.bar(kBarAccFull + s), 1);
-      mbar_init(c.bar(kBarHalf0 + s), epi_per_slot);
-      mbar_init(c.bar(kBarHalf1 + s), epi_per_slot);
       mbar_init(c.bar(kBarDrain + s), 1);
     }
     for (int s = 0; s < kMaxBStages; ++s) mbar_init(c.bar(kBarBEmpty + s), 1);
@@ -926,7 +744,7 @@ __global__ void __launch_bounds__(is_stream(V) ? kFusedThreads : 32 * (kMaxSlotW
   __syncthreads();
   tc_fence_after_sync();
   c.tmem = *tmem_slot;
-  if (!is_stream(V)) {
+  {
     // The constant A slab of every bias MMA: column 0 of every TMEM lane
     // holds (1.0, 0) as an FP16 pair, columns 1..7 zeros.
     if (warp < 4) {
@@ -951,22 +769,16 @@ __global__ void __launch_bounds__(is_stream(V) ? kFusedThreads : 32 * (kMaxSlotW
       bulk_load(c.sbase + p.sm_w + off, p.blob + off, bytes, c.bar(kBarWLoad));
     }
   }
-  const int slot_warps = static_cast<int>(blockDim.x >> 5) - 1;  // the last warp produces inputs
-  if constexpr (is_stream(V)) {
-    if (warp < kCtrlWarps) {
-      if (warp < static_cast<int>(p.n_slots)) {
-        run_slot_control_stream<V>(p, c, warp, lane);
-      } else if (warp == static_cast<int>(p.n_slots) && lane == 0) {
-        run_weight_producer(p, c);
-      }
-      __syncwarp();
-    } else if (warp < slot_warps) {
-      run_epilogue<V>(p, c, warp, lane);
-    }
-  } else {
-    if (warp < slot_warps) run_slot_resident<V>(p, c, warp, lane);
+  // Warps: the slots' warps, then (streamed weights) the weight producer,
+  // then the input producer.
+  const int slot_warps = 4 * static_cast<int>(p.n_slots * p.n_groups);
+  if (warp < slot_warps) {
+    run_slot<V>(p, c, warp, lane);
+  } else if (is_stream(V) && warp == slot_warps) {
+    if (lane == 0) run_weight_producer(p, c);
+    __syncwarp();
   }
-  if (warp == slot_warps) {
+  if (warp == static_cast<int>(blockDim.x >> 5) - 1) {
     if (lane == 0) {
       run_input_producer(p, c);
       wait_drain(c.bar(kBarWLoad), 0, p.status);
@@ -1050,27 +862,18 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
   // slot the accumulator and the A region, plus one shared 32-column block
   // for the ones slab), two input stages per slot before one, two output
   // buffers before one. If the weights do not fit (fused and
-  // scalar-activation variants), stream them with at most 2 slots (two
-  // accumulator regions each; a control warp must stay free to produce) and
-  // the deepest weight ring (4 down to 2 stages) that fits.
+  // scalar-activation variants), stream them with at most 2 slots and the
+  // deepest weight ring (4 down to 2 stages) that fits.
   for (int mode = 0; mode < 2; ++mode) {
     const bool streamed = mode == 1;
     if (streamed && variant == kVarRowMajor) break;
-    if (streamed) {
-      p.region_cols = acc_cols;
-      p.slot_cols = 2u * acc_cols;
-      p.a_col = p.ones_col = 0;
-    } else {
-      p.a_col = acc_cols;
-      p.slot_cols = acc_cols + (((hmax / 2u) + 31u) & ~31u);
-      p.region_cols = 0;
-    }
+    p.a_col = acc_cols;
+    p.slot_cols = acc_cols + (((hmax / 2u) + 31u) & ~31u);
     const uint32_t max_slots = streamed ? static_cast<uint32_t>(kStreamSlots) : static_cast<uint32_t>(kMaxSlots);
     for (uint32_t slots = max_slots; slots >= 1; --slots) {
-      const uint32_t used = slots * p.slot_cols + (streamed ? 0u : 32u);
+      const uint32_t used = slots * p.slot_cols + 32u;
       if (used > 512u) continue;
-      if (streamed && (kEpiWarps % (4 * slots))) continue;
-      const uint32_t groups = streamed ? kEpiWarps / (4u * slots) : (slots >= 3 ? 1u : 4u / slots);
+      const uint32_t groups = slots >= 3 ? 1u : 4u / slots;
       p.n_b_stages = (variant == kVarRowMajor) ? slots : 0u;
       for (uint32_t wst = streamed ? kMaxWStages : 0u; wst >= (streamed ? 2u : 0u); --wst) {
         for (uint32_t depth = 2; depth >= 1; --depth) {
@@ -1099,11 +902,10 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
               uint32_t cols = 32;
               while (cols < used) cols <<= 1;
               p.tmem_cols = cols;
-              p.ones_col = streamed ? 0u : slots * p.slot_cols;
+              p.ones_col = slots * p.slot_cols;
               p.n_slots = slots;
               p.n_groups = groups;
-              p.n_threads = streamed ? static_cast<uint32_t>(kFusedThreads)
-                                     : 32u * (4u * slots * groups + 1u);
+              p.n_threads = 32u * (4u * slots * groups + (streamed ? 2u : 1u));
               p.in_stage_bytes = stage;
               p.n_in_stages = depth;
               p.n_out_bufs = obufs;

@@ -17,12 +17,9 @@ constexpr int kMaxBStages = kMaxSlots;       // row-major ablation: one B stage 
 // Resident weights: each slot's warps (4 TMEM lane quadrants x column groups)
 // run its epilogue and issue its MMAs; then one input-producer warp.
 constexpr int kMaxSlotWarps = 4 * kMaxSlots > 16 ? 4 * kMaxSlots : 16;
-// Streamed weights: 4 control warps (slot MMA issue, weight copies), 16
-// epilogue warps, one input-producer warp.
-constexpr int kCtrlWarps = 4;
-constexpr int kEpiWarps = 16;
+// Streamed weights: the slots' warps (16), one weight-producer warp and one
+// input-producer warp.
 constexpr int kStreamSlots = 2;    // tile slots at most with streamed weights
-constexpr int kFusedThreads = 32 * (kCtrlWarps + kEpiWarps + 1);  // launch maximum
 constexpr int kOutBufs = 2;        // output staging buffers per slot (TMA-store double buffer)
 constexpr int kMaxSlabs = kMaxLayers * (kMaxDim / 16);
 constexpr uint32_t kStatusTimeout = 1u;
@@ -45,9 +42,7 @@ enum BarIndex : int {
   kBarInFull = 0,
   kBarInEmpty = kBarInFull + kMaxInStages,
   kBarAccFull = kBarInEmpty + kMaxInStages,
-  kBarHalf0 = kBarAccFull + kMaxSlots,   // epilogue: first half of the columns done
-  kBarHalf1 = kBarHalf0 + kMaxSlots,     // epilogue: all columns done
-  kBarBEmpty = kBarHalf1 + kMaxSlots,
+  kBarBEmpty = kBarAccFull + kMaxSlots,
   kBarWFull = kBarBEmpty + kMaxBStages,   // streamed-weight ring
   kBarWEmpty = kBarWFull + 4,
   kBarWLoad = kBarWEmpty + 4,
@@ -129,8 +124,6 @@ struct FusedParams {  // 128-byte aligned through its CUtensorMap members
   // the next layer's FP16 A (from a_col); one "ones" slab (8 columns) at
   // ones_col serves every slot's bias MMA.
   uint32_t a_col, ones_col;
-  // Streamed weights: a slot holds two accumulator regions of region_cols.
-  uint32_t region_cols;
   uint32_t stream_w;    // 1: weights streamed through the ring instead of resident
   uint32_t n_wstages;   // streamed-weight ring depth
   uint32_t wstage_bytes;
