@@ -457,8 +457,10 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
     const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(rr) % D;
     const uint32_t b_base = (V == kVarRowMajor) ? b_stage : c.sbase + p.sm_w + li.w_off;
     const uint64_t b_add = b_base >> 4;
-    const uint32_t nslab = li.slab_end - li.slab_begin;
-    const uint32_t tab = c.slab_addr(p, li.slab_begin);
+    // Slab count from the kernel parameters and the table row by layer: the
+    // descriptor loads do not wait for the layer entry.
+    const uint32_t nslab = static_cast<uint32_t>((p.nslab_bits >> (4 * l)) & 15u) + 1u;
+    const uint32_t tab = c.slab_addr(p, 16u * static_cast<uint32_t>(l));
     const uint64_t bias_bd = smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u);
     bool ok = true;
     if (l == 0) {
@@ -800,10 +802,13 @@ __global__ void __launch_bounds__(is_stream(V) ? 32 * (16 + 2) : 32 * (kMaxSlotW
 uint32_t build_schedule(const int32_t* dims, int L, const uint32_t* w_off, const uint32_t* rm_off,
                         Schedule& sc, uint32_t* bslab_bytes) {
   std::memset(&sc, 0, sizeof(sc));
-  uint32_t slab = 0, boff = 0;
+  uint32_t boff = 0;
   for (int l = 0; l < L; ++l) {
     const int K = dims[l], N = dims[l + 1];
     LayerInfo& li = sc.layer[l];
+    // Layer l's k-slabs start at row 16 l of the descriptor table, so the
+    // kernel finds them without first reading the layer's entry.
+    uint32_t slab = static_cast<uint32_t>(l) * 16u;
     li.K = K;
     li.N = N;
     li.slab_begin = slab;
@@ -826,7 +831,7 @@ uint32_t build_schedule(const int32_t* dims, int L, const uint32_t* w_off, const
     boff += align1024(static_cast<uint32_t>(N) * 32u);
   }
   *bslab_bytes = boff;
-  return static_cast<uint32_t>(sizeof(LayerInfo) * kMaxLayers + sizeof(SlabDesc) * slab);
+  return static_cast<uint32_t>(sizeof(LayerInfo) * kMaxLayers + sizeof(SlabDesc) * 16u * L);
 }
 
 uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint32_t smem_optin) {
@@ -843,6 +848,9 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
   p.n_bias = nb;
   p.d0 = dims[0];
   p.dL = dims[L];
+  p.nslab_bits = 0;
+  for (int l = 0; l < L; ++l)
+    p.nslab_bits |= static_cast<uint64_t>((dims[l] >> 4) - 1) << (4 * l);
   const uint32_t acc_cols = (nmax + 31u) & ~31u;  // widest layer, a multiple of 32
   // output staging: 8 KB per 32-column chunk, 4 KB for a trailing 16-column one
   p.out_slot_bytes = static_cast<uint32_t>(p.dL >> 5) * (kTileM * 64u) +

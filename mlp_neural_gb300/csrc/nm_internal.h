@@ -108,6 +108,7 @@ struct FusedParams {  // 128-byte aligned through its CUtensorMap members
   uint32_t n_bias;        // sum of d_1..d_L
   uint32_t sched_bytes;   // bytes of the schedule to copy
   uint32_t bslab_bytes;   // bytes of the bias-slab region
+  uint64_t nslab_bits;    // 4 bits per layer: K_l / 16 - 1
   uint32_t bias_row0[kMaxLayers];  // index of b_l[0] among the concatenated biases
   uint32_t bslab_off[kMaxLayers];  // byte offset of b_l's slab in the bias-slab region
   // shared-memory plan (byte offsets from the 1024-aligned base)
