@@ -20,6 +20,8 @@ SMALL_DIMS = [
     (16, 16),
     (64, 128, 128, 32),
     (32, 48, 96, 208, 16),
+    (256, 128, 16),      # 16 k-slabs in one layer (resident weights)
+    (32,) * 17,          # the most layers a network may have
 ]
 # Networks whose packed weights do not fit in shared memory: the kernel
 # streams their weights (wide: 2 tile slots, heterogeneous: 1).
