@@ -3,31 +3,26 @@
 // One CTA per SM walks 128-sample tiles t = blockIdx.x, blockIdx.x + grid, ...
 // and runs every layer of the network on each tile without leaving the SM
 // ("Optimization Techniques: Squeezing the Silicon", "Kernel Fusion": one
-// write to memory, intermediates stay on chip). Up to four tiles are in
-// flight per CTA (tile slots). A slot owns two TMEM regions, each as wide as
-// the widest layer: the slot's q-th layer evaluation (chain q) accumulates in
-// FP32 in region q & 1, and its epilogue writes the FP16 activations -- the
-// next layer's A operand -- back into the columns of that region it has just
-// read, while chain q + 1 accumulates in the other region. Only the input
-// tile (layer 1's A), the weights, the bias operands and the output staging
-// live in shared memory. Roles, by warp:
-//   warps 0..3   control, one per slot: lane 0 issues every layer's
-//                tcgen05.mma chain for the slot's tiles, D[128 x N] (FP32,
-//                TMEM) = A[128 x K] (FP16; smem for layer 1, TMEM after) *
-//                W^T (smem) + b; the four slots' chains run from four threads
-//                because one thread issues MMAs only about one per 60 cycles.
-//                (With streamed weights, the warp after the last slot's
-//                copies the weights.)
-//   warps 4..19  epilogue, 16 warps split as slots x 4 TMEM lane quadrants x
-//                column groups: tcgen05.ld of the accumulator rows, FP16
-//                rounding, FP16 activation max(h, h*half(0.01)), tcgen05.st
-//                of the FP16 pairs (or, after the last layer, 16-byte stores
-//                into an output staging tile that the same warp sends out by
-//                TMA). The epilogue reports its first half of the columns
-//                separately, so the next layer's MMAs on those k-slabs start
-//                while it works on the second half.
-//   warp 20      input producer: lane 0 keeps every slot's input ring filled
-//                by TMA, off the control threads' critical path.
+// write to memory, intermediates stay on chip). Up to five tiles are in
+// flight per CTA (tile slots; TMEM decides how many). A slot owns a TMEM
+// region holding its FP32 accumulator and, beside it, the FP16 activations
+// that feed the next layer as the tensor core's A operand; the input tile
+// (layer 1's A), the weights, the bias operands and the output staging live in
+// shared memory. Roles, by warp:
+//   slot warps   4 x G per slot (the 4 TMEM lane quadrants x G column
+//                groups). Per layer they wait for the accumulator, read it
+//                (tcgen05.ld), round to FP16, apply max(h, h*half(0.01)) and
+//                write the pairs as the next layer's A (tcgen05.st) -- or,
+//                after the last layer, into an output staging tile each warp
+//                sends out by TMA -- then meet at the slot's named barrier.
+//                One lane of them, chosen by elect.sync, then issues the next
+//                layer's tcgen05.mma chain, D[128 x N] (FP32, TMEM) =
+//                A[128 x K] * W^T + b, and commits it to the slot's
+//                accumulator barrier. With streamed weights that lane also
+//                takes each K-segment from the weight ring.
+//   weight producer (streamed weights only): copies the layers' K-segments
+//                into the shared weight ring.
+//   input producer (last warp): keeps every slot's input ring filled by TMA.
 //
 // The page "Profiling neural material inference" fixes the arithmetic
 // ("Experiment setup": the full layer chain per evaluation; "Bad versus good
@@ -35,9 +30,10 @@
 // here as variants: "Row-major versus InferencingOptimal weights" (B operand
 // rebuilt from row-major memory per tile) and the indexed-lane activation.
 //
-// All UMMA descriptors are precomputed on the host (the schedule) and copied
-// into shared memory once per CTA; a layer's chain loads its descriptors
-// together and issues its MMAs as straight-line sequences.
+// All UMMA descriptors are precomputed on the host (the schedule, one table
+// row per layer) and copied into shared memory once per CTA; a layer's chain
+// loads its descriptors together and issues its MMAs as straight-line
+// sequences.
 //
 // Every wait is bounded by a wall-clock limit. A wait that gives up sets the
 // device status word and a CTA-wide abort flag; every role then stops, waits
@@ -284,7 +280,7 @@ __device__ __forceinline__ int32_t tile_of(int32_t i) {
 // the slots consume them (tile i goes to slot i % S, round i / S), each into
 // its slot's ring stage once the layer-1 MMAs of the round that used the
 // stage D rounds earlier have completed. Issuing a TMA load holds the issuing
-// thread for hundreds of cycles, so no control thread does it.
+// thread for hundreds of cycles, so no lane that issues MMAs does it.
 __device__ __forceinline__ void run_input_producer(const FusedParams& p, const Ctx& c) {
   const int32_t S = static_cast<int32_t>(p.n_slots);
   const uint32_t D = p.n_in_stages;
@@ -636,12 +632,12 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
 
 // ------------------------------------------------------------------ streamed weights
 // Networks whose packed weights do not fit next to the pipeline buffers
-// stream them: a producer thread (an otherwise idle control warp) copies each
-// layer's K-segments -- each a contiguous N x 2w-byte piece of the packed
-// image, at most 32 KB -- into a shared ring, in the order (round, layer,
-// segment) in which every slot's control thread consumes them. A stage is
-// released once every slot's MMAs on it have completed (or, for a slot with
-// no tile in that round, once it has seen the stage).
+// stream them: lane 0 of the weight-producer warp copies each layer's
+// K-segments -- each a contiguous N x 2w-byte piece of the packed image, at
+// most 32 KB -- into a shared ring, in the order (round, layer, segment) in
+// which every slot's issuing lane consumes them. A stage is released once
+// every slot's MMAs on it have completed (or, for a slot with no tile in that
+// round, once its lane has seen the stage).
 
 __device__ __forceinline__ void run_weight_producer(const FusedParams& p, const Ctx& c) {
   const int32_t S = static_cast<int32_t>(p.n_slots);
