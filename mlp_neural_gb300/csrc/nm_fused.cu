@@ -341,11 +341,21 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
   const int32_t S = static_cast<int32_t>(p.n_slots);
   const int G = static_cast<int>(p.n_groups);
   const int nw = 4 * G;  // warps of this slot
-  const int32_t s = warp / nw;
-  const int g = (warp % nw) / 4;
   const int quad = warp & 3;  // TMEM lane quadrant this warp may access
-  const int wi = warp % nw;   // index among the slot's warps
-  const bool issuer_warp = (g == 0) && (quad == (s & 3));
+  // One column group: warp w of group w / 4 serves slot (w / 4 + quad) % S,
+  // so each slot has one warp per quadrant and the slots' issuing warps
+  // (the lowest-numbered warp of each slot) sit at the lowest warp indices.
+  const int32_t s = (G == 1) ? (warp / 4 + quad) % S : warp / nw;
+  const int g = (G == 1) ? 0 : (warp % nw) / 4;
+  const int wi = (G == 1) ? quad : warp % nw;  // index among the slot's warps
+  int iw = 0x7FFFFFFF;
+  if (G == 1) {
+    for (int qq = 0; qq < 4; ++qq) {
+      const int w = 4 * ((s - qq + 4 * S) % S) + qq;
+      iw = w < iw ? w : iw;
+    }
+  }
+  const bool issuer_warp = (G == 1) ? (warp == iw) : ((g == 0) && (quad == (s & 3)));
   const bool issuer = issuer_warp && lane == 0;
   const uint32_t row = static_cast<uint32_t>(quad * 32 + lane);
   const uint32_t lane_bits = static_cast<uint32_t>(quad * 32) << 16;
