@@ -87,6 +87,12 @@ struct nm_mlp {
   size_t mirror_elems = 0;
   bool packed = false;
   bool mirror_valid = false;
+  // A packing kernel (weights or the row-major mirror) was the last of this
+  // handle's launches on `pack_stream`: the next dispatch there must not
+  // overlap it, since the kernel reads the weights before its grid
+  // dependency wait.
+  bool pack_pending = false;
+  cudaStream_t pack_stream = nullptr;
   int variant = nm::kVarFused;
   uint64_t wait_ns = 2000000000ull;
   uint32_t test_stall = 0;
@@ -230,6 +236,8 @@ nm_status ensure_mirror(nm_mlp* h, cudaStream_t stream) {
     pp.rm_b[l] = h->mirror + h->rm_b_off[l];
   }
   if (nm::launch_pack(pp, true, h->num_sms, stream) != cudaSuccess) return NM_ERR_CUDA;
+  h->pack_pending = true;
+  h->pack_stream = stream;
   h->params.mirror = h->mirror;
   h->mirror_valid = true;
   return NM_OK;
@@ -248,7 +256,9 @@ nm_status launch_infer(nm_mlp* h, const void* in, int64_t n, void* out, cudaStre
   const uint32_t smem = nm::plan_fused_smem(p, h->dims, h->variant, h->smem_optin);
   if (smem == 0) return NM_ERR_UNSUPPORTED;
   const int grid = p.num_tiles < h->num_sms ? p.num_tiles : h->num_sms;
-  if (nm::launch_fused(p, h->variant, grid, smem, s) != cudaSuccess) return NM_ERR_CUDA;
+  const bool after_pack = h->pack_pending && s == h->pack_stream;
+  if (nm::launch_fused(p, h->variant, grid, smem, s, !after_pack) != cudaSuccess) return NM_ERR_CUDA;
+  if (after_pack) h->pack_pending = false;
   return NM_OK;
 }
 
@@ -436,6 +446,8 @@ nm_status nm_mlp_pack_weights(nm_mlp* h, const void* const* W, const void* const
     return NM_ERR_CUDA;
   h->packed = true;
   h->mirror_valid = false;
+  h->pack_pending = true;
+  h->pack_stream = reinterpret_cast<cudaStream_t>(stream);
   return NM_OK;
 }
 

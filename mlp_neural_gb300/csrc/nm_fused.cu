@@ -699,6 +699,11 @@ __global__ void __launch_bounds__(is_stream(V) ? 32 * (16 + 2) : 32 * (kMaxSlotW
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(c.gbase + p.sm_bar + kTmemSlotOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // Every CTA of the grid is resident (one per SM, the grid no larger than
+  // the SM count), so the next dispatch may be scheduled now: its CTAs take
+  // the SMs this grid's CTAs leave and run their prologue while the last of
+  // them finish.
+  if (threadIdx.x == 0) griddep_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxInStages; ++s) {
       mbar_init(c.bar(kBarInFull + s), 1);
@@ -777,6 +782,12 @@ __global__ void __launch_bounds__(is_stream(V) ? 32 * (16 + 2) : 32 * (kMaxSlotW
       bulk_load(c.sbase + p.sm_w + off, p.blob + off, bytes, c.bar(kBarWLoad));
     }
   }
+  // Inputs, outputs and the status word may be shared with the previous
+  // kernel of the stream: nothing below touches them before it completes.
+  // The prologue above reads only the packed weights, which no kernel writes
+  // except the packing kernel, and a dispatch that follows a packing kernel
+  // is launched without programmatic serialisation.
+  griddep_wait();
   // Warps: the slots' warps, then (streamed weights) the weight producer,
   // then the input producer.
   const int slot_warps = 4 * static_cast<int>(p.n_slots * p.n_groups);
@@ -938,7 +949,8 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
 }
 
 template <int V>
-static cudaError_t launch_variant(const FusedParams& p, int grid, uint32_t smem, cudaStream_t stream) {
+static cudaError_t launch_variant(const FusedParams& p, int grid, uint32_t smem, cudaStream_t stream,
+                                  bool overlap) {
   static bool configured = false;
   if (!configured) {
     int dev = 0, optin = 0;
@@ -949,21 +961,30 @@ static cudaError_t launch_variant(const FusedParams& p, int grid, uint32_t smem,
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  fused_mlp_kernel<V><<<grid, p.n_threads, smem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(p.n_threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fused_mlp_kernel<V>, p);
 }
 
 cudaError_t launch_fused(const FusedParams& p, int variant, int grid, uint32_t smem,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, bool overlap) {
   if (p.stream_w) {
-    if (variant == kVarFused) return launch_variant<kVarFusedStream>(p, grid, smem, stream);
-    if (variant == kVarScalar) return launch_variant<kVarScalarStream>(p, grid, smem, stream);
+    if (variant == kVarFused) return launch_variant<kVarFusedStream>(p, grid, smem, stream, overlap);
+    if (variant == kVarScalar) return launch_variant<kVarScalarStream>(p, grid, smem, stream, overlap);
     return cudaErrorInvalidValue;
   }
   switch (variant) {
-    case kVarFused: return launch_variant<kVarFused>(p, grid, smem, stream);
-    case kVarRowMajor: return launch_variant<kVarRowMajor>(p, grid, smem, stream);
-    case kVarScalar: return launch_variant<kVarScalar>(p, grid, smem, stream);
+    case kVarFused: return launch_variant<kVarFused>(p, grid, smem, stream, overlap);
+    case kVarRowMajor: return launch_variant<kVarRowMajor>(p, grid, smem, stream, overlap);
+    case kVarScalar: return launch_variant<kVarScalar>(p, grid, smem, stream, overlap);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -136,8 +136,11 @@ struct FusedParams {  // 128-byte aligned through its CUtensorMap members
 // the smem plan of `p`. Returns the dynamic smem bytes, or 0 if no plan fits.
 uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint32_t smem_optin);
 
+// `overlap`: launch with programmatic stream serialisation, so that the
+// kernel's prologue may overlap the end of the previous kernel on `stream`.
+// Only allowed when that previous kernel does not write the packed weights.
 cudaError_t launch_fused(const FusedParams& p, int variant, int grid, uint32_t smem,
-                         cudaStream_t stream);
+                         cudaStream_t stream, bool overlap);
 
 struct PackParams {
   int32_t L;

@@ -207,7 +207,7 @@ extern "C" nm_status nm_mlp_infer_noalloc(const int32_t* dims, int32_t n_dims,
   pp.blob = blob;
   if (nm::launch_pack(pp, false, ds.num_sms, s) != cudaSuccess) return NM_ERR_CUDA;
   const int grid = p.num_tiles < ds.num_sms ? p.num_tiles : ds.num_sms;
-  if (nm::launch_fused(p, nm::kVarFused, grid, smem, s) != cudaSuccess) return NM_ERR_CUDA;
+  if (nm::launch_fused(p, nm::kVarFused, grid, smem, s, false) != cudaSuccess) return NM_ERR_CUDA;
 
   // ---- completion: this entry point returns only once `stream` has run the
   // work, so that a kernel-side give-up can be reported.

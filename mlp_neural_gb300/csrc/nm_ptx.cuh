@@ -23,6 +23,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Programmatic dependent launch. `griddep_launch_dependents` lets the next
+// kernel of the stream, if it was launched with programmatic stream
+// serialisation, be scheduled once every CTA of this grid has executed it or
+// exited; `griddep_wait` blocks until the grids this one depends on have
+// completed and their memory operations are visible (a no-op for a kernel
+// launched without that attribute).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

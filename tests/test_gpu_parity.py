@@ -315,6 +315,79 @@ def test_infer_captured_in_cuda_graph(orc):
     m.close()
 
 
+def _signed_permutation_net(dims, rng, scales):
+    W, b = [], []
+    for l in range(len(dims) - 1):
+        K, N = dims[l], dims[l + 1]
+        w = np.zeros((N, K), np.float16)
+        w[np.arange(N), rng.permutation(K)[:N]] = rng.choice(scales, size=N)
+        W.append(w.view(np.uint16))
+        b.append(np.zeros(N, np.uint16))
+    return W, b
+
+
+@pytest.mark.parametrize("dims", [(64,) * 9, (128,) * 9])
+def test_back_to_back_dispatches_chain_through_buffers(orc, dims):
+    """Dispatches queued back to back on one stream overlap only their
+    prologues: each reads its input after the previous dispatch wrote it, and
+    writes its output after the previous dispatch read it. The network is
+    exact (one product per output), so every link of the chain is bit-exact
+    whatever the others computed."""
+    import torch
+    rng = np.random.default_rng(sum(dims) + 5)
+    W, b = _signed_permutation_net(dims, rng, [-1.0, -0.5, 0.5, 1.0])
+    n = 152 * 128 * 2 + 77  # several tiles per CTA and a ragged tail
+    x = rng.uniform(-1, 1, size=(n, dims[0])).astype(np.float16).view(np.uint16)
+    m = make_net(dims, W, b)
+    X = to_dev(x)
+    A = torch.empty((n, dims[-1]), dtype=torch.float16, device="cuda")
+    B = torch.empty_like(A)
+    m.infer(X, A)  # y1
+    m.infer(A, B)  # y2 = f(y1): reads what the previous dispatch wrote
+    m.infer(B, A)  # y3 = f(y2): overwrites what the previous dispatch read
+    m.infer(A, X)  # y4 = f(y3)
+    torch.cuda.synchronize()
+    assert m.device_status() == nm().NM_OK
+    y1 = orc.forward(dims, W, b, x)
+    y2 = orc.forward(dims, W, b, y1)
+    y3 = orc.forward(dims, W, b, y2)
+    y4 = orc.forward(dims, W, b, y3)
+    assert np.array_equal(to_host(B), y2)
+    assert np.array_equal(to_host(A), y3)
+    assert np.array_equal(to_host(X), y4)
+    m.close()
+
+
+@pytest.mark.parametrize("dims", [synth.WORKLOADS["page"].dims, synth.WORKLOADS["wide"].dims])
+def test_repack_between_dispatches_on_one_stream(orc, dims):
+    """A dispatch queued right after a repack on the same stream uses the new
+    weights, and the one queued before it the old ones."""
+    import torch
+    W1, b1, x = synth.small_net_inputs(dims, seed=41, n=3000)
+    W2, b2, _ = synth.small_net_inputs(dims, seed=42, n=1)
+    m = make_net(dims, W1, b1)
+    dev1 = ([to_dev(w) for w in W1], [to_dev(v) for v in b1])
+    dev2 = ([to_dev(w) for w in W2], [to_dev(v) for v in b2])
+    xd = to_dev(x)
+    outs = [torch.empty((x.shape[0], dims[-1]), dtype=torch.float16, device="cuda")
+            for _ in range(4)]
+    torch.cuda.synchronize()
+    m.infer(xd, outs[0])
+    m.pack_weights(*dev2)
+    m.infer(xd, outs[1])
+    m.infer(xd, outs[2])
+    m.pack_weights(*dev1)
+    m.infer(xd, outs[3])
+    torch.cuda.synchronize()
+    assert m.device_status() == nm().NM_OK
+    y = [to_host(o) for o in outs]
+    assert_close(y[0], orc.forward(dims, W1, b1, x), "before the repack")
+    assert_close(y[1], orc.forward(dims, W2, b2, x), "right after the repack")
+    assert np.array_equal(y[2], y[1])
+    assert np.array_equal(y[3], y[0])
+    m.close()
+
+
 def test_two_handles_on_two_streams(orc):
     """Two networks dispatched concurrently on two streams do not disturb
     each other."""
