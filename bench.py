@@ -391,6 +391,29 @@ def main(argv=None):
     te = max_over_ranks(time.perf_counter() - te0, world, dev)
     e2e_value = whole_job_rate(w.n_evals, E, world, te)
 
+    # the host link's bound on that step: the same input and output bytes
+    # copied alone between the same pinned buffers and device memory, the two
+    # directions concurrently on two streams
+    lin = torch.empty_like(xdev)
+    lout = torch.empty((n, d_out), dtype=torch.float16, device=dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def link_step():
+        with torch.cuda.stream(s_in):
+            lin.copy_(hin, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            hout.copy_(lout, non_blocking=True)
+        torch.cuda.synchronize()
+
+    link_step()
+    link_s = []
+    for _ in range(5):
+        tl0 = time.perf_counter()
+        link_step()
+        link_s.append(time.perf_counter() - tl0)
+    link_ms = sorted(link_s)[2] * 1e3
+    del lin, lout
+
     peaks, peaks_src = load_peaks()
     bound, _, _ = roofline_bound(w, peaks)
     if bound == "tensor":
@@ -414,7 +437,9 @@ def main(argv=None):
                        parallelism=f"replicas x{world}, no collective on the data path"),
         "roofline": roofline,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(hin.numel() * 2),
-                "d2h_bytes_per_step": int(hout.numel() * 2)},
+                "d2h_bytes_per_step": int(hout.numel() * 2),
+                "link_ms_per_step": link_ms,
+                "frac_of_link": link_ms / (te / E * 1e3)},
         "gpu_launches": K,
         "kernel_ms": avg_kernel_ms,
         "pack_ms": pack_ms,
