@@ -414,7 +414,44 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
     if (l == 0)
       ok = wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(rr) / D) & 1u, p.wait_ns,
                       c.abort_flag, p.status);
-    for (int k = 0; k < li.K && ok;) {
+    // 64-wide K-segments (all of them when K is a multiple of 64): the four
+    // k-slab MMAs of each are issued straight-line, with the segment's
+    // descriptors derived from its ring stage alone -- segment j of the
+    // input tile starts 128 x 128 bytes after segment j - 1, and the layer's
+    // A in TMEM 32 columns after.
+    const int n64 = li.K >> 6;
+    const uint64_t desc64 = smem_desc(0u, 1024u, swizzle_code(64));
+    if (l == 0) {
+      for (int j = 0; j < n64 && ok; ++j) {
+        ok = wait_phase(c.bar(kBarWFull + ws), wph, p.wait_ns, c.abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const uint64_t bd = desc64 + ((c.sbase + p.sm_wring + ws * p.wstage_bytes) >> 4);
+        const uint64_t ad = desc64 + ((in_base + 16384u * static_cast<uint32_t>(j)) >> 4);
+        umma_f16_ss(slot_tmem, ad, bd, li.idesc, j > 0 ? 1u : 0u);
+        umma_f16_ss(slot_tmem, ad + 2u, bd + 2u, li.idesc, 1u);
+        umma_f16_ss(slot_tmem, ad + 4u, bd + 4u, li.idesc, 1u);
+        umma_f16_ss(slot_tmem, ad + 6u, bd + 6u, li.idesc, 1u);
+        umma_commit(c.bar(kBarWEmpty + ws));
+        next_stage();
+      }
+    } else {
+      for (int j = 0; j < n64 && ok; ++j) {
+        ok = wait_phase(c.bar(kBarWFull + ws), wph, p.wait_ns, c.abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const uint64_t bd = desc64 + ((c.sbase + p.sm_wring + ws * p.wstage_bytes) >> 4);
+        const uint32_t at = slot_tmem + p.a_col + 32u * static_cast<uint32_t>(j);
+        umma_f16_ts(slot_tmem, at, bd, li.idesc, j > 0 ? 1u : 0u);
+        umma_f16_ts(slot_tmem, at + 8u, bd + 2u, li.idesc, 1u);
+        umma_f16_ts(slot_tmem, at + 16u, bd + 4u, li.idesc, 1u);
+        umma_f16_ts(slot_tmem, at + 24u, bd + 6u, li.idesc, 1u);
+        umma_commit(c.bar(kBarWEmpty + ws));
+        next_stage();
+      }
+    }
+    // The narrower tail segments (K mod 64 = 16, 32 or 48).
+    for (int k = n64 << 6; k < li.K && ok;) {
       uint32_t aoff;
       int w, k0;
       locate(kTileM, li.K, k, aoff, w, k0);

@@ -25,7 +25,9 @@ SMALL_DIMS = [
 ]
 # Networks whose packed weights do not fit in shared memory: the kernel
 # streams their weights (wide: 2 tile slots, heterogeneous: 1).
-STREAMED_DIMS = [synth.WORKLOADS["wide"].dims, synth.WORKLOADS["hetero"].dims]
+STREAMED_DIMS = [synth.WORKLOADS["wide"].dims, synth.WORKLOADS["hetero"].dims,
+                 (48, 240, 208, 176, 16),    # 1 slot; K-segments of 64, 32 and 16
+                 (80,) + (112,) * 8 + (16,)]  # 2 slots; every K leaves a tail
 SENTINEL = 0x7E7E  # a NaN pattern the kernel never produces from finite data
 
 
