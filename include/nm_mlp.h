@@ -134,7 +134,14 @@ nm_status nm_mlp_packed_blob(const nm_mlp *h, const void **blob);
  * Errors: NM_ERR_INVALID_ARG (NULL/misaligned pointers, n < 0 or n > 2^31 - 128),
  * NM_ERR_NOT_PACKED, NM_ERR_UNSUPPORTED (the network does not fit the
  * selected variant's shared-memory budget), NM_ERR_CUDA (launch failure).
- * A kernel-side wait that gives up is reported by nm_mlp_device_status. */
+ * A kernel-side wait that gives up is reported by nm_mlp_device_status.
+ * Stream order: the dispatch is launched with programmatic stream
+ * serialisation. Its set-up (barriers, tensor memory, weight staging) may
+ * run while the previous kernel on `stream` finishes. It reads `in` and
+ * writes `out` only after that kernel has completed, so chaining dispatches
+ * through shared buffers on one stream is safe. A dispatch that directly
+ * follows this handle's nm_mlp_pack_weights on the same stream does not
+ * overlap it. */
 nm_status nm_mlp_infer(nm_mlp *h, const void *in, int64_t n, void *out, nm_stream stream);
 
 /* The same evaluation with the inputs and outputs in HOST memory. The pages

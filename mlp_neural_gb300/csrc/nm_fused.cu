@@ -30,10 +30,17 @@
 // here as variants: "Row-major versus InferencingOptimal weights" (B operand
 // rebuilt from row-major memory per tile) and the indexed-lane activation.
 //
-// All UMMA descriptors are precomputed on the host (the schedule, one table
-// row per layer) and copied into shared memory once per CTA; a layer's chain
-// loads its descriptors together and issues its MMAs as straight-line
-// sequences.
+// With resident weights all UMMA descriptors are precomputed on the host (the
+// schedule, one table row per layer) and copied into shared memory once per
+// CTA; a layer's chain loads its descriptors together and issues its MMAs as
+// straight-line sequences. With streamed weights each 64-wide K-segment's
+// descriptors follow from the ring stage it sits in, and its four MMAs are
+// issued straight-line too.
+//
+// Dispatches overlap on a stream: each CTA lets the next kernel be scheduled
+// as soon as it starts (programmatic dependent launch), and every thread
+// waits on the grid dependency before touching inputs, outputs or the status
+// word, so only the prologue runs alongside the previous kernel.
 //
 // Every wait is bounded by a wall-clock limit. A wait that gives up sets the
 // device status word and a CTA-wide abort flag; every role then stops, waits
@@ -404,8 +411,8 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
   };
   // Streamed weights: the layer's K-segments are taken from the ring as the
   // weight-producer warp fills it, in the (round, layer, segment) order in
-  // which every slot consumes it; each stage is released by a commit once
-  // this slot's MMAs on it complete.
+  // which every slot consumes it, one segment per stage; each stage is
+  // released by a commit once this slot's MMAs on it complete.
   auto issue_stream = [&](int32_t rr, int l) -> bool {
     const LayerRegs li = load_layer(p, c, l);
     const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(rr) % D;

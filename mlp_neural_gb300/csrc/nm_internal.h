@@ -37,15 +37,16 @@ enum Variant : int {
 constexpr int kMaxWStages = 4;     // streamed-weight ring depth (upper bound)
 
 // Barrier slots inside the barrier block of the fused kernel's smem. Input
-// stage s * n_in_stages + k belongs to slot s; likewise B stages 2s, 2s + 1.
+// stage s * n_in_stages + k belongs to slot s; the row-major ablation's B
+// stage s belongs to slot s.
 enum BarIndex : int {
   kBarInFull = 0,
   kBarInEmpty = kBarInFull + kMaxInStages,
   kBarAccFull = kBarInEmpty + kMaxInStages,
   kBarBEmpty = kBarAccFull + kMaxSlots,
   kBarWFull = kBarBEmpty + kMaxBStages,   // streamed-weight ring
-  kBarWEmpty = kBarWFull + 4,
-  kBarWLoad = kBarWEmpty + 4,
+  kBarWEmpty = kBarWFull + kMaxWStages,
+  kBarWLoad = kBarWEmpty + kMaxWStages,
   kBarDrain = kBarWLoad + 1,  // one per slot
   kBarNever = kBarDrain + kMaxSlots,  // never signalled (failure-path test hook)
   kBarCount = kBarNever + 1
