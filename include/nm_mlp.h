@@ -224,6 +224,37 @@ nm_status nm_mlp_infer_noalloc(const int32_t *dims, int32_t n_dims, const void *
                                const void *const *b, const void *in, int64_t n, void *out,
                                nm_stream stream);
 
+/* How the fused kernel runs a network, worked out on the host alone: no
+ * device is touched, so this answers on a machine without a GPU. The kernel
+ * keeps several 128-sample tiles in flight per CTA (tile slots), as many as
+ * tensor memory allows; it keeps the packed weights resident in shared
+ * memory when they fit, and otherwise streams them through a shared ring.
+ * nm_mlp_infer uses the same plan for the same widths, variant and shared
+ * memory limit.
+ * dims, n_dims: as for nm_mlp_create.
+ * variant: the kernel variant (nm_mlp_set_variant).
+ * smem_optin: the device's opt-in shared memory per block, in bytes
+ *   (cudaDevAttrMaxSharedMemoryPerBlockOptin; 232,448 on GB300).
+ * The row-major ablation never stages the packed weights: it rebuilds each
+ * layer's operand per tile, so its plans report streamed_weights = 0.
+ * Errors: NM_ERR_INVALID_ARG (NULL pointer, fewer than two widths, unknown
+ * variant), NM_ERR_UNSUPPORTED (a width or layer count out of range, or no
+ * plan fits in smem_optin; nm_mlp_infer then answers the same). */
+typedef struct nm_plan {
+  int32_t tile_slots;       /* 128-sample tiles in flight per CTA */
+  int32_t warps_per_slot;   /* 4 TMEM lane quadrants x column groups */
+  int32_t threads;          /* per CTA: the slots' warps and the producer warps */
+  int32_t streamed_weights; /* 0: resident in shared memory, 1: streamed */
+  int32_t weight_stages;    /* depth of the streamed-weight ring (0 if resident) */
+  int32_t input_stages;     /* input ring stages per slot */
+  int32_t output_buffers;   /* output staging buffers per slot */
+  uint32_t smem_bytes;      /* dynamic shared memory per CTA */
+  uint32_t tmem_columns;    /* tensor memory columns allocated per CTA */
+} nm_plan;
+
+nm_status nm_mlp_plan(const int32_t *dims, int32_t n_dims, nm_variant variant,
+                      uint32_t smem_optin, nm_plan *plan);
+
 /* Free the handle and its device memory (synchronises the device first).
  * NULL is a no-op. */
 void nm_mlp_destroy(nm_mlp *h);

@@ -327,14 +327,81 @@ const char* nm_status_str(nm_status s) {
   return "NM_ERR_UNKNOWN";
 }
 
-nm_status nm_mlp_create(const int32_t* dims, int32_t n_dims, nm_mlp** out) {
-  if (!out) return NM_ERR_INVALID_ARG;
-  *out = nullptr;
+// Widths d_0..d_L: 1 <= L <= 16, each a multiple of 16 in [16, 256].
+static nm_status check_dims(const int32_t* dims, int32_t n_dims) {
   if (!dims || n_dims < 2) return NM_ERR_INVALID_ARG;
   const int L = n_dims - 1;
   if (L > nm::kMaxLayers) return NM_ERR_UNSUPPORTED;
   for (int l = 0; l <= L; ++l)
     if (dims[l] < 16 || dims[l] > nm::kMaxDim || dims[l] % 16 != 0) return NM_ERR_UNSUPPORTED;
+  return NM_OK;
+}
+
+// Host arithmetic of a network's packed blob: the byte offset of each
+// layer's image (1024-aligned), the element offsets of the row-major mirror,
+// and the FP16 biases after the images. Sets p.L and p.bias_off; returns the
+// blob's size in bytes.
+static size_t net_layout(const int32_t* dims, int L, FusedParams& p, uint32_t* w_off,
+                         uint32_t* rm_off, uint32_t* rm_b_off, size_t* mirror_elems) {
+  p.L = L;
+  uint32_t off = 0;
+  size_t rm = 0;
+  for (int l = 0; l < L; ++l) {
+    off = nm::align1024(off);
+    w_off[l] = off;
+    off += nm::image_bytes(static_cast<uint32_t>(dims[l + 1]), dims[l]);
+    rm_off[l] = static_cast<uint32_t>(rm);
+    rm += static_cast<size_t>(dims[l]) * dims[l + 1];
+  }
+  for (int l = 0; l < L; ++l) {
+    rm_b_off[l] = static_cast<uint32_t>(rm);
+    rm += static_cast<size_t>(dims[l + 1]);
+  }
+  *mirror_elems = rm;
+  p.bias_off = nm::align1024(off);
+  uint32_t nb = 0;
+  for (int l = 0; l < L; ++l) nb += static_cast<uint32_t>(dims[l + 1]);
+  return p.bias_off + 2u * nb;
+}
+
+nm_status nm_mlp_plan(const int32_t* dims, int32_t n_dims, nm_variant variant,
+                      uint32_t smem_optin, nm_plan* plan) {
+  if (!plan) return NM_ERR_INVALID_ARG;
+  if (variant != NM_VARIANT_FUSED && variant != NM_VARIANT_ROWMAJOR_WEIGHTS &&
+      variant != NM_VARIANT_SCALAR_ACTIVATION)
+    return NM_ERR_INVALID_ARG;
+  const nm_status dst = check_dims(dims, n_dims);
+  if (dst != NM_OK) return dst;
+  const int L = n_dims - 1;
+  FusedParams p;
+  std::memset(&p, 0, sizeof(p));
+  uint32_t w_off[nm::kMaxLayers], rm_off[nm::kMaxLayers], rm_b_off[nm::kMaxLayers];
+  size_t mirror_elems = 0;
+  net_layout(dims, L, p, w_off, rm_off, rm_b_off, &mirror_elems);
+  nm::Schedule* sc = new (std::nothrow) nm::Schedule;
+  if (!sc) return NM_ERR_OOM;
+  p.sched_bytes = nm::build_schedule(dims, L, w_off, rm_off, *sc, &p.bslab_bytes);
+  delete sc;
+  const uint32_t smem = nm::plan_fused_smem(p, dims, static_cast<int>(variant), smem_optin);
+  if (smem == 0) return NM_ERR_UNSUPPORTED;
+  plan->tile_slots = static_cast<int32_t>(p.n_slots);
+  plan->warps_per_slot = static_cast<int32_t>(4u * p.n_groups);
+  plan->threads = static_cast<int32_t>(p.n_threads);
+  plan->streamed_weights = p.stream_w ? 1 : 0;
+  plan->weight_stages = p.stream_w ? static_cast<int32_t>(p.n_wstages) : 0;
+  plan->input_stages = static_cast<int32_t>(p.n_in_stages);
+  plan->output_buffers = static_cast<int32_t>(p.n_out_bufs);
+  plan->smem_bytes = smem;
+  plan->tmem_columns = p.tmem_cols;
+  return NM_OK;
+}
+
+nm_status nm_mlp_create(const int32_t* dims, int32_t n_dims, nm_mlp** out) {
+  if (!out) return NM_ERR_INVALID_ARG;
+  *out = nullptr;
+  const nm_status dst = check_dims(dims, n_dims);
+  if (dst != NM_OK) return dst;
+  const int L = n_dims - 1;
 
   int dev = 0, major = 0, minor = 0, sms = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return NM_ERR_CUDA;
@@ -353,26 +420,8 @@ nm_status nm_mlp_create(const int32_t* dims, int32_t n_dims, nm_mlp** out) {
   h->smem_optin = static_cast<uint32_t>(optin);
   FusedParams& p = h->params;
   std::memset(&p, 0, sizeof(p));
-  p.L = L;
-  uint32_t off = 0;
-  size_t rm = 0;
   for (int l = 0; l <= L; ++l) h->dims[l] = dims[l];
-  for (int l = 0; l < L; ++l) {
-    off = nm::align1024(off);
-    h->w_off[l] = off;
-    off += nm::image_bytes(static_cast<uint32_t>(dims[l + 1]), dims[l]);
-    h->rm_off[l] = static_cast<uint32_t>(rm);
-    rm += static_cast<size_t>(dims[l]) * dims[l + 1];
-  }
-  for (int l = 0; l < L; ++l) {
-    h->rm_b_off[l] = static_cast<uint32_t>(rm);
-    rm += static_cast<size_t>(dims[l + 1]);
-  }
-  h->mirror_elems = rm;
-  p.bias_off = nm::align1024(off);
-  uint32_t nb = 0;
-  for (int l = 0; l < L; ++l) nb += static_cast<uint32_t>(dims[l + 1]);
-  h->blob_size = p.bias_off + 2u * nb;
+  h->blob_size = net_layout(dims, L, p, h->w_off, h->rm_off, h->rm_b_off, &h->mirror_elems);
 
   nm::Schedule* sc = new (std::nothrow) nm::Schedule;
   if (!sc) {

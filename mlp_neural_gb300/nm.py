@@ -44,6 +44,7 @@ SIGNATURES = {
     "nm_mlp_set_wait_limit": (ctypes.c_int, [_P, ctypes.c_uint64]),
     "nm_mlp_set_test_stall": (ctypes.c_int, [_P, ctypes.c_int32]),
     "nm_mlp_infer_noalloc": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, _P, ctypes.c_int64, _P, _P]),
+    "nm_mlp_plan": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int, ctypes.c_uint32, _P]),
     "nm_mlp_destroy": (None, [_P]),
 }
 
@@ -100,6 +101,28 @@ def _stream(stream) -> int:
     if isinstance(stream, int):
         return stream
     return int(stream.cuda_stream)
+
+
+class Plan(ctypes.Structure):
+    """nm_plan: how the fused kernel runs a network (see nm_mlp_plan)."""
+    _fields_ = [("tile_slots", ctypes.c_int32), ("warps_per_slot", ctypes.c_int32),
+                ("threads", ctypes.c_int32), ("streamed_weights", ctypes.c_int32),
+                ("weight_stages", ctypes.c_int32), ("input_stages", ctypes.c_int32),
+                ("output_buffers", ctypes.c_int32), ("smem_bytes", ctypes.c_uint32),
+                ("tmem_columns", ctypes.c_uint32)]
+
+
+GB300_SMEM_OPTIN = 232448  # opt-in shared memory per block on GB300, bytes
+
+
+def plan(dims, variant: int = NM_VARIANT_FUSED, smem_optin: int = GB300_SMEM_OPTIN) -> dict:
+    """nm_mlp_plan: the kernel's plan for a network, computed on the host
+    (no device needed). Raises NmError if no plan fits."""
+    d = (ctypes.c_int32 * len(dims))(*[int(v) for v in dims])
+    p = Plan()
+    _check(lib().nm_mlp_plan(d, len(dims), int(variant), int(smem_optin), ctypes.byref(p)),
+           "nm_mlp_plan")
+    return {name: getattr(p, name) for name, _ in Plan._fields_}
 
 
 def infer_noalloc(dims, W, b, x, out, stream=None) -> int:

@@ -1,0 +1,83 @@
+"""The fused kernel's host-side planner through nm_mlp_plan, on the CPU:
+the plans of the benchmark networks, and invariants every plan must hold
+(shared memory within the limit, tensor memory within 512 columns, the
+thread count the roles add up to) over a seeded sweep of networks."""
+import numpy as np
+import pytest
+
+from mlp_neural_gb300 import synth
+
+
+@pytest.fixture(scope="module")
+def nmlib():
+    from mlp_neural_gb300 import build, nm
+    build.build()
+    return nm
+
+
+@pytest.mark.parametrize("name,slots,warps,streamed", [
+    ("tiny", 5, 4, 0), ("page", 5, 4, 0), ("wide", 2, 8, 1), ("hetero", 1, 16, 1)])
+def test_benchmark_network_plans(nmlib, name, slots, warps, streamed):
+    p = nmlib.plan(synth.WORKLOADS[name].dims)
+    assert (p["tile_slots"], p["warps_per_slot"], p["streamed_weights"]) == (slots, warps, streamed)
+    assert p["threads"] == 32 * (slots * warps + 1 + streamed)
+    assert p["weight_stages"] == (4 if streamed else 0)
+    assert p["smem_bytes"] <= nmlib.GB300_SMEM_OPTIN and p["tmem_columns"] == 512
+
+
+def _tmem_needed(dims, slots):
+    # per slot: the FP32 accumulator of the widest layer and the FP16 pairs of
+    # the widest hidden layer (each rounded up to 32 columns), plus one
+    # 32-column block for the shared ones slab
+    r32 = lambda c: (c + 31) // 32 * 32
+    acc = r32(max(dims[1:]))
+    hidden = max([16] + list(dims[1:-1]))
+    return slots * (acc + r32(hidden // 2)) + 32
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2])
+def test_plan_invariants_over_random_networks(nmlib, variant):
+    rng = np.random.default_rng(100 + variant)
+    planned = 0
+    for _ in range(400):
+        L = int(rng.integers(1, 17))
+        dims = [int(16 * rng.integers(1, 17)) for _ in range(L + 1)]
+        try:
+            p = nmlib.plan(dims, variant)
+        except nmlib.NmError as e:
+            assert e.status == nmlib.NM_ERR_UNSUPPORTED
+            continue
+        planned += 1
+        slots, warps = p["tile_slots"], p["warps_per_slot"]
+        assert 1 <= slots <= 5 and warps % 4 == 0
+        assert p["threads"] == 32 * (slots * warps + 1 + p["streamed_weights"]) <= 1024
+        assert p["smem_bytes"] <= nmlib.GB300_SMEM_OPTIN
+        t = p["tmem_columns"]
+        assert 32 <= t <= 512 and t & (t - 1) == 0
+        assert _tmem_needed(dims, slots) <= t
+        assert p["input_stages"] in (1, 2) and p["output_buffers"] in (1, 2)
+        if p["streamed_weights"]:
+            assert variant != 1 and slots <= 2 and 2 <= p["weight_stages"] <= 4
+        else:
+            assert p["weight_stages"] == 0
+    assert planned > 200
+
+
+def test_smaller_shared_memory_limit_gives_a_smaller_plan(nmlib):
+    dims = synth.WORKLOADS["page"].dims
+    big = nmlib.plan(dims)
+    small = nmlib.plan(dims, smem_optin=100 * 1024)
+    assert small["smem_bytes"] <= 100 * 1024
+    assert small["tile_slots"] <= big["tile_slots"]
+
+
+def test_plan_argument_errors(nmlib):
+    with pytest.raises(nmlib.NmError) as e:
+        nmlib.plan((32, 24))
+    assert e.value.status == nmlib.NM_ERR_UNSUPPORTED
+    with pytest.raises(nmlib.NmError) as e:
+        nmlib.plan((32, 16), variant=7)
+    assert e.value.status == nmlib.NM_ERR_INVALID_ARG
+    with pytest.raises(nmlib.NmError) as e:
+        nmlib.plan((32,))
+    assert e.value.status == nmlib.NM_ERR_INVALID_ARG
