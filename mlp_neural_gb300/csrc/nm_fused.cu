@@ -743,10 +743,10 @@ __global__ void __launch_bounds__(is_stream(V) ? 32 * (16 + 2) : 32 * (kMaxSlotW
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(c.gbase + p.sm_bar + kTmemSlotOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // Every CTA of the grid is resident (one per SM, the grid no larger than
-  // the SM count), so the next dispatch may be scheduled now: its CTAs take
-  // the SMs this grid's CTAs leave and run their prologue while the last of
-  // them finish.
+  // The next dispatch may be scheduled now. It launches once every CTA of
+  // this grid has executed this (so all of them are running and will
+  // finish); its CTAs then take the SMs this grid's CTAs leave and run their
+  // prologue while the last of them finish.
   if (threadIdx.x == 0) griddep_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxInStages; ++s) {
