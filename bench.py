@@ -45,6 +45,9 @@ def parse_args(argv=None):
     ap.add_argument("--variant", choices=tuple(VARIANTS), default="fused")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the K timed dispatches in one CUDA graph and replay it (the "
+                         "steady state of back-to-back dispatches without host launch costs)")
     ap.add_argument("--evals", type=int, default=0,
                     help="evaluate only the first EVALS rows of the workload (smaller profiling "
                          "captures; the JSON line's config says so)")
@@ -94,10 +97,35 @@ def load_traffic(workload: str, variant: str):
     return d.get("dram_bytes_per_launch")
 
 
-def roofline_bound(w, peaks):
-    t_tensor = w.flops_per_eval / (peaks["bf16_tflops"] * 1e12)
+def roofline_bound(w, peaks, tensor_tflops=None):
+    tf = tensor_tflops if tensor_tflops else peaks["bf16_tflops"]
+    t_tensor = w.flops_per_eval / (tf * 1e12)
     t_hbm = w.hbm_bytes_per_eval / (peaks["hbm_gbs"] * 1e9)
     return ("tensor" if t_tensor >= t_hbm else "hbm"), t_tensor, t_hbm
+
+
+def measure_fp16_peak(dev, size=8192, reps=10):
+    """Dense FP16 tensor throughput of this GPU, measured the way the BF16
+    figure of the peaks file was: torch.matmul of two FP16 size x size
+    matrices (2 size^3 FLOPs each, FP32 accumulation inside cuBLAS), best of
+    `reps` CUDA-event timings after a warm-up. Returns TFLOP/s."""
+    import torch
+    a = torch.randn((size, size), device=dev, dtype=torch.float16)
+    b = torch.randn((size, size), device=dev, dtype=torch.float16)
+    c = torch.empty((size, size), device=dev, dtype=torch.float16)
+    for _ in range(3):
+        torch.matmul(a, b, out=c)
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.matmul(a, b, out=c)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1e-3)
+    del a, b, c
+    return 2.0 * size ** 3 / best / 1e12
 
 
 # ---------------------------------------------------------------- clocks
@@ -178,15 +206,32 @@ def _oracle_sample(w, n_evals: int):
     return W, b, np.ascontiguousarray(x)
 
 
-def oracle_rate(w, n_evals: int):
-    """Time the oracle, as it stands, on the first n_evals rows of a dispatch."""
+def oracle_rate(w, n_evals: int, threads: int = 1):
+    """Time the oracle, as it stands, on the first n_evals rows of a dispatch.
+    With threads > 1 the rows are cut into contiguous ranges, each range one
+    call of the (single-threaded) oracle, run on a thread pool: ctypes
+    releases the GIL during the call, so the ranges run on that many cores."""
     import oracle
     oracle.build()
     W, b, x = _oracle_sample(w, n_evals)
     t0 = time.perf_counter()
-    oracle.forward(w.dims, W, b, x)
+    if threads <= 1:
+        oracle.forward(w.dims, W, b, x)
+    else:
+        from concurrent.futures import ThreadPoolExecutor
+        step = max(1, math.ceil(n_evals / (4 * threads)))
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(lambda r0: oracle.forward(w.dims, W, b, x[r0:r0 + step]),
+                        range(0, n_evals, step)))
     dt = time.perf_counter() - t0
     return n_evals / dt / 1e6, dt
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
 def run_reference(args, w, rank):
@@ -197,27 +242,35 @@ def run_reference(args, w, rank):
     import oracle
     oracle.build()
     K, W = args.steps if args.steps is not None else default_steps(w), args.warmup
+    cores = host_cores()
     _, dt = oracle_rate(w, 256)
-    per_eval = dt / 256
-    per_step = int(max(16, min(65536, 120.0 / (per_eval * max(1, K + W)))))
+    per_eval = dt / 256 / cores
+    per_step = int(max(16 * cores, min(65536 * cores, 120.0 / (per_eval * max(1, K + W)))))
     Wt, bt, x = _oracle_sample(w, per_step)
-    for _ in range(W):
-        oracle.forward(w.dims, Wt, bt, x)
-    t_total = 0.0
-    for _ in range(K):
-        t0 = time.perf_counter()
-        oracle.forward(w.dims, Wt, bt, x)
-        t_total += time.perf_counter() - t0
+    from concurrent.futures import ThreadPoolExecutor
+    span = math.ceil(per_step / cores)
+    starts = range(0, per_step, span)
+    with ThreadPoolExecutor(cores) as ex:
+        def step():
+            list(ex.map(lambda r0: oracle.forward(w.dims, Wt, bt, x[r0:r0 + span]), starts))
+        for _ in range(W):
+            step()
+        t_total = 0.0
+        for _ in range(K):
+            t0 = time.perf_counter()
+            step()
+            t_total += time.perf_counter() - t0
     value = per_step * K / t_total / 1e6
     sample = (f"{per_step} of the {w.n_evals:,} evaluations of one dispatch per step "
-              f"(first rows), single thread")
+              f"(first rows), {cores} threads each running the single-threaded oracle on "
+              f"its own contiguous rows")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": K, "warmup": W, "ms_per_step": t_total / K * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
         "config": workload_config(w),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -340,6 +393,27 @@ def main(argv=None):
     if m.device_status(stream) != nm.NM_OK:
         raise RuntimeError("device status after warm-up")
 
+    # dense FP16 tensor peak of this GPU, measured before the timed region
+    fp16_tflops = measure_fp16_peak(dev) if rank == 0 else None
+    torch.cuda.synchronize()
+
+    graph = None
+    if args.graph:
+        # the K dispatches captured once (after the eager warm-up above has
+        # done every one-time launch set-up), replayed as one graph launch
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(K):
+                st = m.infer_raw(ins[i % nsets].data_ptr(), n, outs[i % nsets].data_ptr(), cap)
+                if st != nm.NM_OK:
+                    raise nm.NmError(st, "nm_mlp_infer (capture)")
+        stream.wait_stream(cap)
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+
     # the K dispatches go back to back between two events on their stream
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -350,8 +424,11 @@ def main(argv=None):
     torch.cuda.synchronize()
     t0 = time.time()
     ev0.record(stream)
-    for i in range(K):
-        launch(i)
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(K):
+            launch(i)
     ev1.record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
@@ -415,19 +492,25 @@ def main(argv=None):
     del lin, lout
 
     peaks, peaks_src = load_peaks()
-    bound, _, _ = roofline_bound(w, peaks)
+    bound, _, _ = roofline_bound(w, peaks, fp16_tflops)
     if bound == "tensor":
         achieved = w.flops_per_eval * n / (avg_kernel_ms * 1e-3) / 1e12
-        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
+        if fp16_tflops:
+            peak, src = fp16_tflops, ("measured in this run: dense FP16 burst (torch.matmul FP16 "
+                                      "8192^3, best of 10, CUDA events)")
+        else:
+            peak, src = peaks["bf16_tflops"], f"{peaks_src}: dense bf16 burst"
+        unit = "TFLOP/s"
     else:
         achieved = w.hbm_bytes_per_eval * n / (avg_kernel_ms * 1e-3) / 1e9
-        peak, unit = peaks["hbm_gbs"], "GB/s"
+        peak, unit, src = peaks["hbm_gbs"], "GB/s", f"{peaks_src}: HBM copy bandwidth"
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak,
                 "traffic": None if args.evals else load_traffic(w.name, args.variant),
-                "kernel": "fused_mlp_kernel", "peak_source": (
-                    f"{peaks_src}: " + ("dense bf16 burst (FP16 dense has the same nominal rate)"
-                                        if bound == "tensor" else "HBM copy bandwidth"))}
+                "kernel": "fused_mlp_kernel", "peak_source": src,
+                "frac_of_bf16_peaks_file": (achieved / peaks["bf16_tflops"]
+                                            if bound == "tensor" else None),
+                "fp16_dense_tflops_measured": fp16_tflops}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
@@ -443,16 +526,26 @@ def main(argv=None):
         "gpu_launches": K,
         "kernel_ms": avg_kernel_ms,
         "pack_ms": pack_ms,
+        "launch": "one CUDA graph of the K dispatches" if graph is not None else
+                  "K eager dispatches back to back on one stream",
     }
     if sampler:
         line["clocks"] = sampler.summary(t0, t1)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sample_n = min(131072, w.n_evals)
-        v, dt = oracle_rate(w, sample_n)
+        # the oracle on every host core (its per-sample function unchanged,
+        # contiguous row ranges on a thread pool), and on one core
+        cores = host_cores()
+        scale = 57344 / w.flops_per_eval  # about the same CPU time per workload
+        all_n = min(w.n_evals, max(65536, int(1048576 * scale * cores / 16)))
+        v, dt = oracle_rate(w, all_n, threads=cores)
+        one_n = min(w.n_evals, max(16384, int(131072 * scale)))
+        v1, dt1 = oracle_rate(w, one_n)
         line["cpu_baseline"] = {
-            "value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"first {sample_n:,} of the {w.n_evals:,} evaluations of one dispatch, "
-                      f"single thread, {dt:.1f} s"}
+            "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {all_n:,} of the {w.n_evals:,} evaluations of one dispatch, "
+                      f"{cores} threads, {dt:.1f} s",
+            "single_thread": {"value": v1, "unit": UNIT, "cores": 1,
+                              "sample": f"first {one_n:,} evaluations, one thread, {dt1:.1f} s"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     m.close()

@@ -212,13 +212,14 @@ nm_status nm_mlp_set_test_stall(nm_mlp *h, int32_t enable);
  * NM_ERR_UNSUPPORTED (the page-shaped network needs 58,272; the widest
  * 256-wide 16-layer network would need about 2 MB).
  * The first call on a device looks up that array's device address with the
- * device current (a one-time set-up); make that first call before any stream
- * capture. All calls share the array and it keeps the last call's contents
- * (each call clears what must start at zero): calls whose work overlaps on the
- * GPU -- from several host threads, or on several streams -- race and must
- * not be made.
+ * device current (a one-time set-up). All calls share the array and it keeps
+ * the last call's contents (each call clears what must start at zero): calls
+ * whose work overlaps on the GPU -- from several host threads, or on several
+ * streams -- race and must not be made.
  * The call returns after `stream` has completed the work (it synchronises the
  * stream), so a kernel-side give-up is reported directly as NM_ERR_TIMEOUT.
+ * Because it synchronises, it refuses a stream that is being captured into a
+ * CUDA graph: it then returns NM_ERR_UNSUPPORTED before enqueuing anything.
  * Errors: NM_ERR_INVALID_ARG, NM_ERR_UNSUPPORTED, NM_ERR_CUDA, NM_ERR_TIMEOUT. */
 nm_status nm_mlp_infer_noalloc(const int32_t *dims, int32_t n_dims, const void *const *W,
                                const void *const *b, const void *in, int64_t n, void *out,

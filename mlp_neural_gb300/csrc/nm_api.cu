@@ -67,6 +67,132 @@ cudaError_t launch_pack(const PackParams& p, bool unpack, int num_sms, cudaStrea
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- host helpers
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+nm_status get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? NM_OK : NM_ERR_CUDA;
+}
+
+// 2-D map over a row-major FP16 [rows][width] matrix; box = [box_rows][box_w]
+// with the swizzle that matches a box_w-wide segment.
+nm_status encode_map(CUtensorMap* m, const void* ptr, int width, int64_t rows, int box_w,
+                     int box_rows) {
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(width) * 2u};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_w), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estride[2] = {1, 1};
+  const CUtensorMapSwizzle sw = box_w == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : box_w == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_32B;
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), gdim,
+                              gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NM_OK : NM_ERR_CUDA;
+}
+
+}  // namespace
+
+nm_status check_dims(const int32_t* dims, int32_t n_dims) {
+  if (!dims || n_dims < 2) return NM_ERR_INVALID_ARG;
+  const int L = n_dims - 1;
+  if (L > kMaxLayers) return NM_ERR_UNSUPPORTED;
+  for (int l = 0; l <= L; ++l)
+    if (dims[l] < 16 || dims[l] > kMaxDim || dims[l] % 16 != 0) return NM_ERR_UNSUPPORTED;
+  return NM_OK;
+}
+
+size_t net_layout(const int32_t* dims, int L, FusedParams& p, uint32_t* w_off, uint32_t* rm_off,
+                  uint32_t* rm_b_off, size_t* mirror_elems) {
+  p.L = L;
+  uint32_t off = 0;
+  size_t rm = 0;
+  for (int l = 0; l < L; ++l) {
+    off = align1024(off);
+    w_off[l] = off;
+    off += image_bytes(static_cast<uint32_t>(dims[l + 1]), dims[l]);
+    if (rm_off) rm_off[l] = static_cast<uint32_t>(rm);
+    rm += static_cast<size_t>(dims[l]) * dims[l + 1];
+  }
+  for (int l = 0; l < L; ++l) {
+    if (rm_b_off) rm_b_off[l] = static_cast<uint32_t>(rm);
+    rm += static_cast<size_t>(dims[l + 1]);
+  }
+  if (mirror_elems) *mirror_elems = rm;
+  p.bias_off = align1024(off);
+  uint32_t nb = 0;
+  for (int l = 0; l < L; ++l) nb += static_cast<uint32_t>(dims[l + 1]);
+  return p.bias_off + 2u * nb;
+}
+
+void set_bias_params(const Schedule& sc, const int32_t* dims, int L, FusedParams& p) {
+  uint32_t row0 = 0;
+  for (int l = 0; l < L; ++l) {
+    p.bias_row0[l] = row0;
+    p.bslab_off[l] = sc.layer[l].bslab_off;
+    row0 += static_cast<uint32_t>(dims[l + 1]);
+  }
+  p.n_bias = row0;
+}
+
+nm_status encode_io_maps(FusedParams& p, const int32_t* dims, int L, const void* in, void* out,
+                         int64_t n) {
+  nm_status st = get_encoder();
+  if (st != NM_OK) return st;
+  std::memset(p.tm_in, 0, sizeof(p.tm_in));
+  std::memset(p.tm_out, 0, sizeof(p.tm_out));
+  int w[16], k0[16];
+  const int ns = segments(dims[0], w, k0);
+  for (int s = 0; s < ns; ++s) {
+    st = encode_map(&p.tm_in[swizzle_kind(w[s])], in, dims[0], n, w[s], kTileM);
+    if (st != NM_OK) return st;
+  }
+  // Output: 32-row boxes of 32 columns (64-byte swizzle), plus 16 columns
+  // (32-byte swizzle) for a trailing 16-column chunk.
+  const int dl = dims[L];
+  if (dl >= 32) {
+    st = encode_map(&p.tm_out[swizzle_kind(32)], out, dl, n, 32, 32);
+    if (st != NM_OK) return st;
+  }
+  if (dl & 31) {
+    st = encode_map(&p.tm_out[swizzle_kind(16)], out, dl, n, 16, 32);
+    if (st != NM_OK) return st;
+  }
+  return NM_OK;
+}
+
+PackParams make_pack_params(const int32_t* dims, int L, const uint32_t* w_off, uint32_t bias_off,
+                            uint8_t* blob) {
+  PackParams pp;
+  std::memset(&pp, 0, sizeof(pp));
+  pp.L = L;
+  uint32_t cw = 0, cb = 0;
+  for (int l = 0; l <= L; ++l) pp.dims[l] = dims[l];
+  for (int l = 0; l < L; ++l) {
+    pp.w_off[l] = w_off[l];
+    pp.chunk_start[l] = cw;
+    pp.bias_chunk_start[l] = cb;
+    cw += static_cast<uint32_t>(dims[l] * dims[l + 1] / 8);
+    cb += static_cast<uint32_t>(dims[l + 1] / 8);
+  }
+  pp.chunk_start[L] = cw;
+  pp.bias_chunk_start[L] = cb;
+  pp.bias_off = bias_off;
+  pp.blob = blob;
+  return pp;
+}
+
 }  // namespace nm
 
 using nm::FusedParams;
@@ -124,44 +250,14 @@ struct nm_mlp {
 
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+using nm::aligned16;
+using nm::kMaxRows;
 
 constexpr int kHostStreams = 3;
-constexpr int64_t kMaxRows = (static_cast<int64_t>(1) << 31) - 128;
 
-nm_status get_encoder() {
-  std::call_once(g_encode_once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  return g_encode ? NM_OK : NM_ERR_CUDA;
-}
-
-// 2-D map over a row-major FP16 [rows][width] matrix; box = [box_rows][box_w]
-// with the swizzle that matches a box_w-wide segment.
-nm_status encode_map(CUtensorMap* m, const void* ptr, int width, int64_t rows, int box_w,
-                     int box_rows) {
-  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(rows)};
-  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(width) * 2u};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_w), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estride[2] = {1, 1};
-  const CUtensorMapSwizzle sw = box_w == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
-                                : box_w == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                              : CU_TENSOR_MAP_SWIZZLE_32B;
-  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), gdim,
-                              gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? NM_OK : NM_ERR_CUDA;
-}
-
-nm_status encode_io_maps(nm_mlp* h, const void* in, void* out, int64_t n) {
+// I/O tensor maps for (in, out, n), from the handle's cache of recent
+// triples when possible.
+nm_status cached_io_maps(nm_mlp* h, const void* in, void* out, int64_t n) {
   FusedParams& p = h->params;
   for (int i = 0; i < nm_mlp::kMapCache; ++i) {
     const nm_mlp::MapEntry& e = h->maps[i];
@@ -171,27 +267,8 @@ nm_status encode_io_maps(nm_mlp* h, const void* in, void* out, int64_t n) {
       return NM_OK;
     }
   }
-  nm_status st = get_encoder();
+  const nm_status st = nm::encode_io_maps(p, h->dims, h->L, in, out, n);
   if (st != NM_OK) return st;
-  std::memset(p.tm_in, 0, sizeof(p.tm_in));
-  std::memset(p.tm_out, 0, sizeof(p.tm_out));
-  int w[16], k0[16];
-  int ns = nm::segments(h->dims[0], w, k0);
-  for (int s = 0; s < ns; ++s) {
-    st = encode_map(&p.tm_in[nm::swizzle_kind(w[s])], in, h->dims[0], n, w[s], nm::kTileM);
-    if (st != NM_OK) return st;
-  }
-  // Output: 32-row boxes of 32 columns (64-byte swizzle), plus 16 columns
-  // (32-byte swizzle) for a trailing 16-column chunk.
-  const int dl = h->dims[h->L];
-  if (dl >= 32) {
-    st = encode_map(&p.tm_out[nm::swizzle_kind(32)], out, dl, n, 32, 32);
-    if (st != NM_OK) return st;
-  }
-  if (dl & 31) {
-    st = encode_map(&p.tm_out[nm::swizzle_kind(16)], out, dl, n, 16, 32);
-    if (st != NM_OK) return st;
-  }
   nm_mlp::MapEntry& e = h->maps[h->map_next];
   h->map_next = (h->map_next + 1) % nm_mlp::kMapCache;
   std::memcpy(e.tm_in, p.tm_in, sizeof(p.tm_in));
@@ -203,23 +280,7 @@ nm_status encode_io_maps(nm_mlp* h, const void* in, void* out, int64_t n) {
 }
 
 PackParams make_pack_params(const nm_mlp* h) {
-  PackParams pp;
-  std::memset(&pp, 0, sizeof(pp));
-  pp.L = h->L;
-  uint32_t cw = 0, cb = 0;
-  for (int l = 0; l <= h->L; ++l) pp.dims[l] = h->dims[l];
-  for (int l = 0; l < h->L; ++l) {
-    pp.w_off[l] = h->w_off[l];
-    pp.chunk_start[l] = cw;
-    pp.bias_chunk_start[l] = cb;
-    cw += static_cast<uint32_t>(h->dims[l] * h->dims[l + 1] / 8);
-    cb += static_cast<uint32_t>(h->dims[l + 1] / 8);
-  }
-  pp.chunk_start[h->L] = cw;
-  pp.bias_chunk_start[h->L] = cb;
-  pp.bias_off = h->params.bias_off;
-  pp.blob = h->blob;
-  return pp;
+  return nm::make_pack_params(h->dims, h->L, h->w_off, h->params.bias_off, h->blob);
 }
 
 nm_status ensure_mirror(nm_mlp* h, cudaStream_t stream) {
@@ -246,7 +307,7 @@ nm_status ensure_mirror(nm_mlp* h, cudaStream_t stream) {
 // Encodes the I/O tensor maps for (in, out, n) and launches the fused kernel
 // on `s`. Arguments are already checked.
 nm_status launch_infer(nm_mlp* h, const void* in, int64_t n, void* out, cudaStream_t s) {
-  nm_status st = encode_io_maps(h, in, out, n);
+  nm_status st = cached_io_maps(h, in, out, n);
   if (st != NM_OK) return st;
   FusedParams& p = h->params;
   p.n = n;
@@ -327,57 +388,20 @@ const char* nm_status_str(nm_status s) {
   return "NM_ERR_UNKNOWN";
 }
 
-// Widths d_0..d_L: 1 <= L <= 16, each a multiple of 16 in [16, 256].
-static nm_status check_dims(const int32_t* dims, int32_t n_dims) {
-  if (!dims || n_dims < 2) return NM_ERR_INVALID_ARG;
-  const int L = n_dims - 1;
-  if (L > nm::kMaxLayers) return NM_ERR_UNSUPPORTED;
-  for (int l = 0; l <= L; ++l)
-    if (dims[l] < 16 || dims[l] > nm::kMaxDim || dims[l] % 16 != 0) return NM_ERR_UNSUPPORTED;
-  return NM_OK;
-}
-
-// Host arithmetic of a network's packed blob: the byte offset of each
-// layer's image (1024-aligned), the element offsets of the row-major mirror,
-// and the FP16 biases after the images. Sets p.L and p.bias_off; returns the
-// blob's size in bytes.
-static size_t net_layout(const int32_t* dims, int L, FusedParams& p, uint32_t* w_off,
-                         uint32_t* rm_off, uint32_t* rm_b_off, size_t* mirror_elems) {
-  p.L = L;
-  uint32_t off = 0;
-  size_t rm = 0;
-  for (int l = 0; l < L; ++l) {
-    off = nm::align1024(off);
-    w_off[l] = off;
-    off += nm::image_bytes(static_cast<uint32_t>(dims[l + 1]), dims[l]);
-    rm_off[l] = static_cast<uint32_t>(rm);
-    rm += static_cast<size_t>(dims[l]) * dims[l + 1];
-  }
-  for (int l = 0; l < L; ++l) {
-    rm_b_off[l] = static_cast<uint32_t>(rm);
-    rm += static_cast<size_t>(dims[l + 1]);
-  }
-  *mirror_elems = rm;
-  p.bias_off = nm::align1024(off);
-  uint32_t nb = 0;
-  for (int l = 0; l < L; ++l) nb += static_cast<uint32_t>(dims[l + 1]);
-  return p.bias_off + 2u * nb;
-}
-
 nm_status nm_mlp_plan(const int32_t* dims, int32_t n_dims, nm_variant variant,
                       uint32_t smem_optin, nm_plan* plan) {
   if (!plan) return NM_ERR_INVALID_ARG;
   if (variant != NM_VARIANT_FUSED && variant != NM_VARIANT_ROWMAJOR_WEIGHTS &&
       variant != NM_VARIANT_SCALAR_ACTIVATION)
     return NM_ERR_INVALID_ARG;
-  const nm_status dst = check_dims(dims, n_dims);
+  const nm_status dst = nm::check_dims(dims, n_dims);
   if (dst != NM_OK) return dst;
   const int L = n_dims - 1;
   FusedParams p;
   std::memset(&p, 0, sizeof(p));
   uint32_t w_off[nm::kMaxLayers], rm_off[nm::kMaxLayers], rm_b_off[nm::kMaxLayers];
   size_t mirror_elems = 0;
-  net_layout(dims, L, p, w_off, rm_off, rm_b_off, &mirror_elems);
+  nm::net_layout(dims, L, p, w_off, rm_off, rm_b_off, &mirror_elems);
   nm::Schedule* sc = new (std::nothrow) nm::Schedule;
   if (!sc) return NM_ERR_OOM;
   p.sched_bytes = nm::build_schedule(dims, L, w_off, rm_off, *sc, &p.bslab_bytes);
@@ -399,7 +423,7 @@ nm_status nm_mlp_plan(const int32_t* dims, int32_t n_dims, nm_variant variant,
 nm_status nm_mlp_create(const int32_t* dims, int32_t n_dims, nm_mlp** out) {
   if (!out) return NM_ERR_INVALID_ARG;
   *out = nullptr;
-  const nm_status dst = check_dims(dims, n_dims);
+  const nm_status dst = nm::check_dims(dims, n_dims);
   if (dst != NM_OK) return dst;
   const int L = n_dims - 1;
 
@@ -421,7 +445,7 @@ nm_status nm_mlp_create(const int32_t* dims, int32_t n_dims, nm_mlp** out) {
   FusedParams& p = h->params;
   std::memset(&p, 0, sizeof(p));
   for (int l = 0; l <= L; ++l) h->dims[l] = dims[l];
-  h->blob_size = net_layout(dims, L, p, h->w_off, h->rm_off, h->rm_b_off, &h->mirror_elems);
+  h->blob_size = nm::net_layout(dims, L, p, h->w_off, h->rm_off, h->rm_b_off, &h->mirror_elems);
 
   nm::Schedule* sc = new (std::nothrow) nm::Schedule;
   if (!sc) {
@@ -429,15 +453,7 @@ nm_status nm_mlp_create(const int32_t* dims, int32_t n_dims, nm_mlp** out) {
     return NM_ERR_OOM;
   }
   p.sched_bytes = nm::build_schedule(h->dims, L, h->w_off, h->rm_off, *sc, &p.bslab_bytes);
-  {
-    uint32_t row0 = 0;
-    for (int l = 0; l < L; ++l) {
-      p.bias_row0[l] = row0;
-      p.bslab_off[l] = sc->layer[l].bslab_off;
-      row0 += static_cast<uint32_t>(dims[l + 1]);
-    }
-    p.n_bias = row0;
-  }
+  nm::set_bias_params(*sc, dims, L, p);
 
   if (cudaMalloc(&h->blob, h->blob_size) != cudaSuccess) {
     delete sc;

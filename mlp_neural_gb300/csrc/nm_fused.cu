@@ -48,7 +48,9 @@
 // frees its tensor memory and exits.
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <cstring>
+#include <mutex>
 
 #include "nm_internal.h"
 #include "nm_ptx.cuh"
@@ -743,11 +745,6 @@ __global__ void __launch_bounds__(is_stream(V) ? 32 * (16 + 2) : 32 * (kMaxSlotW
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(c.gbase + p.sm_bar + kTmemSlotOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // The next dispatch may be scheduled now. It launches once every CTA of
-  // this grid has executed this (so all of them are running and will
-  // finish); its CTAs then take the SMs this grid's CTAs leave and run their
-  // prologue while the last of them finish.
-  if (threadIdx.x == 0) griddep_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxInStages; ++s) {
       mbar_init(c.bar(kBarInFull + s), 1);
@@ -801,6 +798,14 @@ __global__ void __launch_bounds__(is_stream(V) ? 32 * (16 + 2) : 32 * (kMaxSlotW
   __syncthreads();
   tc_fence_after_sync();
   c.tmem = *tmem_slot;
+  // The next dispatch of the stream may be scheduled now. It launches once
+  // every CTA of this grid has executed this, that is once every one of them
+  // is running and holds its tensor memory; its CTAs then take the SMs this
+  // grid's CTAs leave and run their prologue while the last of them finish.
+  // A CTA of the next grid that lands on an SM beside one of this grid can
+  // therefore only ever wait for tensor memory that a running CTA of this
+  // grid holds and will free: the waits cannot form a cycle.
+  if (threadIdx.x == 0) griddep_launch_dependents();
   {
     // The constant A slab of every bias MMA: column 0 of every TMEM lane
     // holds (1.0, 0) as an FP16 pair, columns 1..7 zeros.
@@ -992,19 +997,36 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
   return 0;
 }
 
+// The opt-in shared-memory limit of a kernel instantiation is a property of
+// the function in one device's context: it is set once per device (the
+// device current at launch), under a lock so that host threads launching
+// concurrently do not race on it.
+constexpr int kMaxDevices = 64;
+
+template <int V>
+static cudaError_t configure_for_device() {
+  static std::atomic<bool> done[kMaxDevices];
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  int optin = 0;
+  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fused_mlp_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
+  return e;
+}
+
 template <int V>
 static cudaError_t launch_variant(const FusedParams& p, int grid, uint32_t smem, cudaStream_t stream,
                                   bool overlap) {
-  static bool configured = false;
-  if (!configured) {
-    int dev = 0, optin = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(fused_mlp_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  const cudaError_t e = configure_for_device<V>();
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(p.n_threads);

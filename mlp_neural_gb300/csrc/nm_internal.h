@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include "nm_layout.cuh"
+#include "nm_mlp.h"
 
 namespace nm {
 
@@ -156,5 +157,40 @@ struct PackParams {
 };
 
 cudaError_t launch_pack(const PackParams& p, bool unpack, int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------- host helpers
+// Shared by every entry point that launches the kernels (nm_api.cu for the
+// handle-based calls, nm_noalloc.cu for the allocation-free one), so that the
+// network layout, the tensor maps and the pack parameters have one
+// definition.
+
+constexpr int64_t kMaxRows = (static_cast<int64_t>(1) << 31) - 128;  // largest n per dispatch
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Widths d_0..d_L: 1 <= L <= 16, each a multiple of 16 in [16, 256].
+nm_status check_dims(const int32_t* dims, int32_t n_dims);
+
+// Byte offset of each layer's packed image (1024-aligned), element offsets
+// of the row-major mirror, and the FP16 biases after the images. Sets p.L and
+// p.bias_off; returns the blob's size in bytes. rm_off, rm_b_off and
+// mirror_elems may be null.
+size_t net_layout(const int32_t* dims, int L, FusedParams& p, uint32_t* w_off, uint32_t* rm_off,
+                  uint32_t* rm_b_off, size_t* mirror_elems);
+
+// Kernel parameters that follow from the schedule: the first row of each
+// layer's bias among the concatenated biases, each layer's bias-slab offset,
+// and their total count.
+void set_bias_params(const Schedule& sc, const int32_t* dims, int L, FusedParams& p);
+
+// Input maps [n][d_0] (128-row boxes, one per K-segment width) and output
+// maps [n][d_L] (32-row boxes of 32 and/or 16 columns) into p.tm_in / p.tm_out.
+nm_status encode_io_maps(FusedParams& p, const int32_t* dims, int L, const void* in, void* out,
+                         int64_t n);
+
+// Pack-kernel parameters for a network laid out by net_layout; the row-major
+// source (or unpack destination) pointers are left null for the caller.
+PackParams make_pack_params(const int32_t* dims, int L, const uint32_t* w_off, uint32_t bias_off,
+                            uint8_t* blob);
 
 }  // namespace nm

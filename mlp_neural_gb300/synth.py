@@ -112,6 +112,9 @@ WORKLOADS = {
     "ablation": Workload(
         "ablation", (48, 64, 64, 64, 64, 64, 64, 64, 16), seed=1, n_unique=65536, repeats=16,
         description="the page-shaped network and inputs x 16 = 1,048,576 evals (layout/activation ablations)"),
+    "tiny_ablation": Workload(
+        "tiny_ablation", (32, 32, 32, 32, 32, 32, 32, 32, 16), seed=0, n_unique=65536, repeats=16,
+        description="the tiny network and its inputs x 16 = 1,048,576 evals (layout/activation ablations)"),
     "wide": Workload(
         "wide", (64, 128, 128, 128, 128, 128, 128, 128, 16), seed=3, n_unique=16777216,
         description="64->128x7->16, 16,777,216 U(-1,1) inputs, one pass, seed 3"),

@@ -78,3 +78,38 @@ def assert_close(gpu16: np.ndarray, cpu16: np.ndarray, what=""):
     assert bad.size == 0, (f"{what}: {len(bad)} elements outside |gpu-cpu| <= 1e-2 + 1e-2|cpu|; "
                            f"first {bad[:5].tolist()} gpu={g[tuple(bad[0])]} cpu={c[tuple(bad[0])]}")
     return float(err.max()) if err.size else 0.0
+
+
+def check_rows_parallel(orc, dims, W, b, x, y_gpu, chunk=32768, threads=None):
+    """Every row of y_gpu (uint16 FP16 bits, [n, d_L]) against the oracle on
+    the same inputs, within |gpu - cpu| <= 1e-2 + 1e-2|cpu| per element.
+
+    The oracle stays single-threaded per call; contiguous row ranges run on a
+    thread pool over all host cores (ctypes releases the GIL during the call),
+    and each worker compares its own range, so memory stays bounded. Returns
+    (rows checked, largest |gpu - cpu|, threads used)."""
+    from concurrent.futures import ThreadPoolExecutor
+    n = x.shape[0]
+    assert y_gpu.shape == (n, dims[-1])
+    if threads is None:
+        threads = os.cpu_count() or 1
+
+    def work(r0):
+        r1 = min(n, r0 + chunk)
+        ref = orc.forward(dims, W, b, x[r0:r1]).view(np.float16).astype(np.float64)
+        got = y_gpu[r0:r1].view(np.float16).astype(np.float64)
+        err = np.abs(got - ref)
+        bad = ~(err <= TOL_ABS + TOL_REL * np.abs(ref))
+        first = None
+        if bad.any():
+            i, j = np.argwhere(bad)[0]
+            first = (r0 + int(i), int(j), float(got[i, j]), float(ref[i, j]))
+        return int(bad.sum()), first, float(err.max()) if err.size else 0.0
+
+    with ThreadPoolExecutor(threads) as ex:
+        res = list(ex.map(work, range(0, n, chunk)))
+    n_bad = sum(r[0] for r in res)
+    firsts = [r[1] for r in res if r[1] is not None]
+    assert n_bad == 0, (f"{n_bad} elements outside |gpu-cpu| <= 1e-2 + 1e-2|cpu|; "
+                        f"first (row, col, gpu, cpu) = {firsts[0]}")
+    return n, max(r[2] for r in res), threads

@@ -19,8 +19,8 @@ def test_reference_arm_line(capsys):
     assert line["config"]["workload"] == "tiny"
     assert line["config"]["dims"] == list(synth.WORKLOADS["tiny"].dims)
     cb = line["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == line["value"]
-    assert "single thread" in cb["sample"]
+    assert cb["kind"] == "oracle" and cb["cores"] == bench.host_cores() and cb["value"] == line["value"]
+    assert "threads" in cb["sample"]
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
