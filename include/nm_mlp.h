@@ -243,8 +243,11 @@ nm_status nm_mlp_infer_noalloc(const int32_t *dims, int32_t n_dims, const void *
  * plan fits in smem_optin; nm_mlp_infer then answers the same). */
 typedef struct nm_plan {
   int32_t tile_slots;       /* 128-sample tiles in flight per CTA */
-  int32_t warps_per_slot;   /* 4 TMEM lane quadrants x column groups */
-  int32_t threads;          /* per CTA: the slots' warps and the producer warps */
+  int32_t warps_per_slot;   /* epilogue warps: 4 TMEM lane quadrants x column groups */
+  int32_t threads;          /* per CTA. Resident weights: 8 warps (one issuing warp per
+                               slot, the input producer, the rest idle) plus the slots'
+                               epilogue warps. Streamed weights: the slots' warps (which
+                               also issue), the weight producer and the input producer. */
   int32_t streamed_weights; /* 0: resident in shared memory, 1: streamed */
   int32_t weight_stages;    /* depth of the streamed-weight ring (0 if resident) */
   int32_t input_stages;     /* input ring stages per slot */

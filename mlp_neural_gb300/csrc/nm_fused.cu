@@ -110,6 +110,11 @@ __device__ __forceinline__ LayerRegs load_layer(const FusedParams& p, const Ctx&
   return r;
 }
 
+// Output width of layer l, from the kernel parameters.
+__device__ __forceinline__ int layer_n(const FusedParams& p, int l) {
+  return (static_cast<int>((p.n16_bits >> (4 * l)) & 15u) + 1) * 16;
+}
+
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;
   asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.b32 %0, 1, 0, P;\n\t}" : "=r"(pred));
@@ -117,18 +122,27 @@ __device__ __forceinline__ bool elect_one() {
 }
 
 // Bounded wait on an mbarrier phase. Gives up (and raises the abort flag and
-// the status word) when `limit_ns` passes or another role has given up.
+// the status word) when `limit_ns` passes or another role has given up. The
+// abort flag and the clock are looked at once every 64 polls (the clock
+// starts at the 64th), so a poll that does not see the phase complete costs
+// one try_wait: the flag is in shared memory, and a shared-memory load by a
+// warp that has just issued MMAs waits for their operand reads.
 __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                              volatile uint32_t* abort_flag, uint32_t* status) {
-  const uint64_t t0 = globaltimer_ns();
+  uint64_t t0 = 0;
   uint32_t spins = 0;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if ((++spins & 63u) == 0u && globaltimer_ns() - t0 > limit_ns) {
-      *abort_flag = 1u;
-      atomicOr(status, kStatusTimeout);
-      return false;
+    if ((++spins & 63u) == 0u) {
+      if (*abort_flag) return false;
+      const uint64_t now = globaltimer_ns();
+      if (spins == 64u) {
+        t0 = now;
+      } else if (now - t0 > limit_ns) {
+        *abort_flag = 1u;
+        atomicOr(status, kStatusTimeout);
+        return false;
+      }
     }
   }
 }
@@ -222,13 +236,24 @@ __device__ __forceinline__ bool mma_seq_ss(uint32_t d, uint32_t tab, uint64_t a_
 
 // Same with A in TMEM (resident-weight layout: k-slab k of the activations
 // starts 8 columns, 16 FP16 values per row, after slab k - 1); only the B
-// descriptors are fetched.
-template <int NS>
-__device__ __forceinline__ void mma_seq_ts(uint32_t d, uint32_t a_tmem, uint32_t tab, uint64_t b_add,
-                                           uint32_t idesc) {
+// descriptors are needed. The first four of them arrive already loaded
+// (`pre`, fetched before the slot's barrier, off the critical path); the rest
+// are fetched here.
+struct PreDesc {
+  uint2 b0, b1, b2, b3;
+};
+
+template <int NS, bool kPre = true>
+__device__ __forceinline__ void mma_seq_ts(uint32_t d, uint32_t a_tmem, uint32_t tab, PreDesc pre,
+                                           uint64_t b_add, uint32_t idesc) {
   uint2 bd[NS];
 #pragma unroll
-  for (int k = 0; k < NS; ++k) bd[k] = ld_shared_u32x2_ordered(tab + 16u * k + 8u);
+  for (int k = 0; k < NS; ++k)
+    bd[k] = (kPre && k == 0) ? pre.b0
+          : (kPre && k == 1) ? pre.b1
+          : (kPre && k == 2) ? pre.b2
+          : (kPre && k == 3) ? pre.b3
+                             : ld_shared_u32x2_ordered(tab + 16u * k + 8u);
 #pragma unroll
   for (int k = 0; k < NS; ++k)
     umma_f16_ts(d, a_tmem + 8u * k, (static_cast<uint64_t>(bd[k].y) << 32 | bd[k].x) + b_add, idesc,
@@ -254,12 +279,14 @@ __device__ __forceinline__ bool mma_chain_ss(uint32_t nslab, uint32_t d, uint32_
   }
 }
 
+template <bool kPre = true>
 __device__ __forceinline__ void mma_chain_ts(uint32_t nslab, uint32_t d, uint32_t a_tmem,
-                                             uint32_t tab, uint64_t b_add, uint32_t idesc) {
+                                             uint32_t tab, PreDesc pre, uint64_t b_add,
+                                             uint32_t idesc) {
   switch (nslab) {
 #define NM_CASE(n) \
   case n:          \
-    mma_seq_ts<n>(d, a_tmem, tab, b_add, idesc); \
+    mma_seq_ts<n, kPre>(d, a_tmem, tab, pre, b_add, idesc); \
     break;
     NM_SLAB_COUNTS(NM_CASE)
 #undef NM_CASE
@@ -325,7 +352,7 @@ __device__ __forceinline__ uint32_t out_chunk_off(int c0) {
   return static_cast<uint32_t>(c0 >> 5) * (kTileM * 64u);
 }
 
-// ------------------------------------------------------------------ resident weights
+// ------------------------------------------------------------------ streamed weights: slots
 // Tile slot s is served by its own 4G warps (4 TMEM lane quadrants x G column
 // groups). Per layer evaluation (chain) they wait for the accumulator, round
 // and activate it into the slot's A region in TMEM (or, after the last layer,
@@ -524,7 +551,7 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
       ok = mma_chain_ss(nslab, slot_tmem, tab, a_add, b_add, li.idesc, wait);
     } else {
       tc_fence_after_sync();
-      mma_chain_ts(nslab, slot_tmem, slot_tmem + p.a_col, tab, b_add, li.idesc);
+      mma_chain_ts<false>(nslab, slot_tmem, slot_tmem + p.a_col, tab, PreDesc{}, b_add, li.idesc);
     }
     if (ok) {
       umma_f16_ts(slot_tmem, c.tmem + p.ones_col, bias_bd, li.idesc, 1u);
@@ -555,7 +582,11 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
     // Hidden layers: accumulator -> FP16 -> activation -> next layer's A.
     for (int l = 0; l < L - 1; ++l) {
       const uint32_t q = static_cast<uint32_t>(r * L + l);
-      const int N = load_layer(p, c, l).N;  // fetched before the wait
+      // The width comes from the kernel parameters, not from the schedule in
+      // shared memory: a shared-memory load issued by the warp that has just
+      // issued the previous chain's MMAs waits until those MMAs have read
+      // their shared-memory operands, which would hold that warp back.
+      const int N = layer_n(p, l);
       if (ok) ok = warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c);
       if (ok) {
         tc_fence_after_sync();
@@ -686,6 +717,276 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
   if (storer) bulk_wait_group_all();
 }
 
+// ------------------------------------------------------------------ resident weights
+// With resident weights each tile slot has one issuing warp and 4G epilogue
+// warps that meet at the slot's named barrier once per layer evaluation
+// (chain): the epilogue warps arrive when they have turned the accumulator
+// into the next layer's A (or into the output staging tile), the issuing
+// warp arrives when it is ready to issue the next chain. A warp that issues
+// MMAs stays busy for several hundred cycles after its commit (the MMAs'
+// issue, the warp's reconvergence, the loop), so the issuing warp does no
+// epilogue work: its overhead runs while the epilogue warps work, and all of
+// them wait for the accumulator together instead of one of them arriving
+// late at every layer.
+//
+// Both sides pass the same sequence of barriers whatever happens (one at the
+// start, one after every chain's epilogue): a failed wait only turns the
+// remaining work off (`ok`), so no warp is ever left at a barrier that the
+// others have stepped past. A wait that gives up raises the CTA's abort
+// flag, which ends the other side's waits too.
+
+// The issuing warp of slot s: issues chain (r, l) -- K/16 MMAs plus the bias
+// MMA, committed to the slot's accumulator barrier -- after the barrier that
+// follows chain (r, l - 1)'s epilogue (or, for l = 0, round r - 1's last
+// epilogue). Layer 1 reads the input tile from shared memory once it has
+// landed; later layers read A from TMEM, and their descriptors are fetched
+// before the barrier.
+template <int V>
+__device__ __forceinline__ void run_issuer(const FusedParams& p, const Ctx& c, int32_t s, int lane) {
+  const int32_t S = static_cast<int32_t>(p.n_slots);
+  const int L = p.L;
+  const uint32_t D = p.n_in_stages;
+  const int32_t n_rounds = (c.n_local - s + S - 1) / S;
+  const uint32_t slot_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
+  const uint32_t bar_id = 1u + static_cast<uint32_t>(s);
+  const uint32_t bar_threads = 32u * (4u * p.n_groups + 1u);
+  const uint32_t b_stage = c.sbase + p.sm_b + static_cast<uint32_t>(s) * p.b_stage_bytes;
+
+  // Everything a chain on A in TMEM needs that does not depend on the
+  // epilogue: the layer's entry and its first B descriptors.
+  struct IssuePrep {
+    uint64_t b_add, bias_bd;
+    uint32_t idesc, nslab, tab;
+    PreDesc bd;
+  };
+  auto prep_ts = [&](int l) -> IssuePrep {
+    IssuePrep ip;
+    const LayerRegs li = load_layer(p, c, l);
+    ip.idesc = li.idesc;
+    ip.b_add = ((V == kVarRowMajor) ? b_stage : c.sbase + p.sm_w + li.w_off) >> 4;
+    ip.bias_bd = smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u);
+    ip.nslab = static_cast<uint32_t>((p.nslab_bits >> (4 * l)) & 15u) + 1u;
+    ip.tab = c.slab_addr(p, 16u * static_cast<uint32_t>(l));
+    // Rows past the layer's last slab still lie inside the table (16 rows
+    // per layer), so this fixed-count prefetch stays in bounds.
+    ip.bd.b0 = ld_shared_u32x2_ordered(ip.tab + 8u);
+    ip.bd.b1 = ld_shared_u32x2_ordered(ip.tab + 24u);
+    ip.bd.b2 = ld_shared_u32x2_ordered(ip.tab + 40u);
+    ip.bd.b3 = ld_shared_u32x2_ordered(ip.tab + 56u);
+    return ip;
+  };
+  auto fire_ts = [&](const IssuePrep& ip) {
+    tc_fence_after_sync();
+    mma_chain_ts(ip.nslab, slot_tmem, slot_tmem + p.a_col, ip.tab, ip.bd, ip.b_add, ip.idesc);
+    umma_f16_ts(slot_tmem, c.tmem + p.ones_col, ip.bias_bd, ip.idesc, 1u);
+    umma_commit(c.bar(kBarAccFull + s));
+  };
+  // Layer 1 of round rr: A is the input tile in the slot's ring stage.
+  auto issue_first = [&](int32_t rr) -> bool {
+    const LayerRegs li = load_layer(p, c, 0);
+    const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(rr) % D;
+    const uint32_t b_base = (V == kVarRowMajor) ? b_stage : c.sbase + p.sm_w + li.w_off;
+    const uint32_t nslab = static_cast<uint32_t>(p.nslab_bits & 15u) + 1u;
+    const uint64_t a_add = (c.sbase + p.sm_in + st * p.in_stage_bytes) >> 4;
+    auto wait = [&]() -> bool {
+      return wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(rr) / D) & 1u, p.wait_ns,
+                        c.abort_flag, p.status);
+    };
+    if (!mma_chain_ss(nslab, slot_tmem, c.slab_addr(p, 0u), a_add, b_base >> 4, li.idesc, wait))
+      return false;
+    umma_f16_ts(slot_tmem, c.tmem + p.ones_col,
+                smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u), li.idesc, 1u);
+    umma_commit(c.bar(kBarAccFull + s));
+    umma_commit(c.bar(kBarInEmpty + st));
+    return true;
+  };
+
+  bool ok = warp_wait(c.bar(kBarWLoad), 0, p, c);
+  if (ok && p.test_stall) {
+    bool iok = true;
+    if (lane == 0) iok = wait_phase(c.bar(kBarNever), 0, p.wait_ns, c.abort_flag, p.status);
+    ok = __shfl_sync(0xFFFFFFFFu, iok, 0);
+  }
+  if (n_rounds > 0) {
+    named_bar_sync(bar_id, bar_threads);  // the epilogue warps are set up
+    IssuePrep ip;
+    for (int32_t r = 0; r < n_rounds; ++r) {
+      for (int l = 0; l < L; ++l) {
+        // Chain (r, l) ...
+        if (l == 0) {
+          if (ok) {
+            bool iok = true;
+            if (elect_one()) iok = issue_first(r);
+            ok = __all_sync(0xFFFFFFFFu, iok);
+          }
+        } else {
+          if (ok && elect_one()) fire_ts(ip);
+          __syncwarp();
+        }
+        // ... then, while its epilogue runs, the next chain's descriptors
+        // (layers after the first), and the barrier after that epilogue.
+        if (l + 1 < L) ip = prep_ts(l + 1);
+        tc_fence_before_sync();
+        named_bar_sync(bar_id, bar_threads);
+      }
+    }
+  }
+  // Drain: every MMA this warp issued completes before the CTA may exit (the
+  // lane elect.sync picks here is the one that issued them).
+  if (elect_one()) {
+    umma_commit(c.bar(kBarDrain + s));
+    wait_drain(c.bar(kBarDrain + s), 0, p.status);
+  }
+  __syncwarp();
+}
+
+// Epilogue warp e of the resident-weight roles (slot e / 4G, lane quadrant
+// e % 4, column group (e % 4G) / 4): per chain it waits for the slot's
+// accumulator, reads its columns (tcgen05.ld), rounds to FP16 and applies
+// max(h, h * half(0.01)) for a hidden layer, writing the FP16 pairs as the
+// next layer's A (tcgen05.st); after the last layer it writes its rows into
+// the output staging tile and sends them out by TMA once the slot has met.
+template <int V>
+__device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c, int e, int lane) {
+  const int32_t S = static_cast<int32_t>(p.n_slots);
+  const int G = static_cast<int>(p.n_groups);
+  const int nw = 4 * G;             // epilogue warps of a slot
+  const int32_t s = e / nw;
+  const int wi = e % nw;            // index among the slot's epilogue warps
+  const int g = wi / 4;             // column group
+  const int quad = e & 3;           // TMEM lane quadrant (kEpiWarp0 is a multiple of 4)
+  const uint32_t row = static_cast<uint32_t>(quad * 32 + lane);
+  const uint32_t lane_bits = static_cast<uint32_t>(quad * 32) << 16;
+  const uint32_t tbase = c.tmem + static_cast<uint32_t>(s) * p.slot_cols + lane_bits;
+  const uint32_t a_tmem = tbase + p.a_col;
+  const uint32_t bar_id = 1u + static_cast<uint32_t>(s);
+  const uint32_t bar_threads = 32u * static_cast<uint32_t>(nw + 1);
+  const __half2 slope2 = __float2half2_rn(0.01f);  // half(0.01)
+  const int L = p.L;
+  const int n_out = p.dL;
+  const int32_t n_rounds = (c.n_local - s + S - 1) / S;  // tiles r*S + s < n_local
+  const bool storer = (lane == 0) && (32 * g < n_out);
+  const uint32_t b_stage = c.sbase + p.sm_b + static_cast<uint32_t>(s) * p.b_stage_bytes;
+
+  // Row-major ablation: this warp's share (rows wi, wi + nw, ...) of W_l
+  // rebuilt in the slot's B stage, 16-byte loads, swizzled 16-byte stores.
+  auto rebuild_b = [&](int l) {
+    const LayerRegs li = load_layer(p, c, l);
+    const int K = li.K, N = li.N, kc = K >> 3;
+    const uint16_t* Wl = p.mirror + li.rm_off;
+    for (int idx = wi * 32 + lane; idx < N * kc; idx += 32 * nw) {
+      const int n = idx / kc, col = (idx - n * kc) << 3;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(Wl + n * K + col));
+      uint32_t off;
+      int w, k0;
+      locate(static_cast<uint32_t>(N), K, col, off, w, k0);
+      st_shared_v4(b_stage + off + swz(static_cast<uint32_t>(n * 2 * w + (col - k0) * 2), w), v.x,
+                   v.y, v.z, v.w);
+    }
+    fence_proxy_async_smem();  // generic-proxy stores -> MMA reads (async proxy)
+  };
+
+  bool ok = warp_wait(c.bar(kBarWLoad), 0, p, c);
+  if (n_rounds > 0) {
+    if (V == kVarRowMajor && ok) rebuild_b(0);
+    named_bar_sync(bar_id, bar_threads);
+  }
+  for (int32_t r = 0; r < n_rounds; ++r) {
+    const int32_t t = tile_of(r * S + s);
+    // Hidden layers: accumulator -> FP16 -> activation -> next layer's A.
+    for (int l = 0; l < L - 1; ++l) {
+      const uint32_t q = static_cast<uint32_t>(r * L + l);
+      const int N = layer_n(p, l);
+      if (ok) ok = warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c);
+      if (ok) {
+        tc_fence_after_sync();
+        for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
+          uint32_t acc[32], h[16];
+          tmem_ld_x32(tbase + static_cast<uint32_t>(c0), acc);
+          tmem_wait_ld();
+          convert_pairs<V, 16, true>(acc, slope2, h);
+          tmem_st_x16(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
+        }
+        if ((N & 31) && ((N >> 5) % G) == g) {
+          const int c0 = N - 16;
+          uint32_t acc[16], h[8];
+          tmem_ld_x16(tbase + static_cast<uint32_t>(c0), acc);
+          tmem_wait_ld();
+          convert_pairs<V, 8, true>(acc, slope2, h);
+          tmem_st_x8(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
+        }
+        if (V == kVarRowMajor) rebuild_b(l + 1);
+        tmem_wait_st();
+      }
+      tc_fence_before_sync();
+      named_bar_sync(bar_id, bar_threads);
+    }
+    // Last layer: accumulator -> FP16 -> output staging -> TMA store.
+    {
+      const int l = L - 1;
+      const uint32_t q = static_cast<uint32_t>(r * L + l);
+      const int N = n_out;
+      const uint32_t out_dst =
+          c.sbase + p.sm_out +
+          (static_cast<uint32_t>(s) * p.n_out_bufs + static_cast<uint32_t>(r) % p.n_out_bufs) *
+              p.out_slot_bytes;
+      // This staging buffer went to this warp's TMA stores n_out_bufs tiles
+      // of this slot ago; they must have finished reading it.
+      if (storer) {
+        if (p.n_out_bufs > 1)
+          bulk_wait_group_read<1>();
+        else
+          bulk_wait_group_read<0>();
+      }
+      __syncwarp();
+      if (ok) ok = warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c);
+      if (ok) {
+        tc_fence_after_sync();
+        for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
+          uint32_t acc[32], h[16];
+          tmem_ld_x32(tbase + static_cast<uint32_t>(c0), acc);
+          tmem_wait_ld();
+          convert_pairs<V, 16, false>(acc, slope2, h);
+          const uint32_t base = out_dst + out_chunk_off(c0);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            st_shared_v4_nc(base + swz(row * 64u + cc * 16u, 32), h[4 * cc], h[4 * cc + 1],
+                            h[4 * cc + 2], h[4 * cc + 3]);
+        }
+        if ((N & 31) && ((N >> 5) % G) == g) {
+          const int c0 = N - 16;
+          uint32_t acc[16], h[8];
+          tmem_ld_x16(tbase + static_cast<uint32_t>(c0), acc);
+          tmem_wait_ld();
+          convert_pairs<V, 8, false>(acc, slope2, h);
+          const uint32_t base = out_dst + out_chunk_off(c0);
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc)
+            st_shared_v4_nc(base + swz(row * 32u + cc * 16u, 16), h[4 * cc], h[4 * cc + 1],
+                            h[4 * cc + 2], h[4 * cc + 3]);
+        }
+        if (V == kVarRowMajor && r + 1 < n_rounds) rebuild_b(0);
+        fence_proxy_async_smem();  // staging tile -> TMA store (async proxy)
+      }
+      tc_fence_before_sync();
+      named_bar_sync(bar_id, bar_threads);
+      if (storer && ok) {
+        const int64_t row0 = static_cast<int64_t>(t) * kTileM + quad * 32;
+        if (row0 < p.n) {
+          for (int c0 = 32 * g; c0 < N; c0 += 32 * G) {
+            const int cols = (N - c0 >= 32) ? 32 : 16;
+            tma_store_2d(&p.tm_out[swizzle_kind(cols)],
+                         out_dst + out_chunk_off(c0) + static_cast<uint32_t>(quad * 32 * 2 * cols),
+                         c0, static_cast<int32_t>(row0));
+          }
+        }
+      }
+      if (storer) bulk_commit_group();
+    }
+  }
+  if (storer) bulk_wait_group_all();
+}
+
 // ------------------------------------------------------------------ streamed weights
 // Networks whose packed weights do not fit next to the pipeline buffers
 // stream them: lane 0 of the weight-producer warp copies each layer's
@@ -728,7 +1029,7 @@ __device__ __forceinline__ void run_weight_producer(const FusedParams& p, const 
 }
 
 template <int V>
-__global__ void __launch_bounds__(is_stream(V) ? 32 * (16 + 2) : 32 * (kMaxSlotWarps + 1), 1)
+__global__ void __launch_bounds__(is_stream(V) ? 32 * (16 + 2) : 32 * kMaxResidentWarps, 1)
     fused_mlp_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -837,21 +1138,38 @@ __global__ void __launch_bounds__(is_stream(V) ? 32 * (16 + 2) : 32 * (kMaxSlotW
   // except the packing kernel, and a dispatch that follows a packing kernel
   // is launched without programmatic serialisation.
   griddep_wait();
-  // Warps: the slots' warps, then (streamed weights) the weight producer,
-  // then the input producer.
-  const int slot_warps = 4 * static_cast<int>(p.n_slots * p.n_groups);
-  if (warp < slot_warps) {
-    run_slot<V>(p, c, warp, lane);
-  } else if (is_stream(V) && warp == slot_warps) {
-    if (lane == 0) run_weight_producer(p, c);
-    __syncwarp();
-  }
-  if (warp == static_cast<int>(blockDim.x >> 5) - 1) {
-    if (lane == 0) {
-      run_input_producer(p, c);
-      wait_drain(c.bar(kBarWLoad), 0, p.status);
+  if constexpr (is_stream(V)) {
+    // Streamed weights: the slots' warps, then the weight producer, then the
+    // input producer.
+    const int slot_warps = 4 * static_cast<int>(p.n_slots * p.n_groups);
+    if (warp < slot_warps) {
+      run_slot<V>(p, c, warp, lane);
+    } else if (warp == slot_warps) {
+      if (lane == 0) run_weight_producer(p, c);
+      __syncwarp();
     }
-    __syncwarp();
+    if (warp == static_cast<int>(blockDim.x >> 5) - 1) {
+      if (lane == 0) {
+        run_input_producer(p, c);
+        wait_drain(c.bar(kBarWLoad), 0, p.status);
+      }
+      __syncwarp();
+    }
+  } else {
+    // Resident weights: the slots' issuing warps, the input producer, then
+    // (from kEpiWarp0) the slots' epilogue warps.
+    const int S = static_cast<int>(p.n_slots);
+    if (warp < S) {
+      run_issuer<V>(p, c, warp, lane);
+    } else if (warp == S) {
+      if (lane == 0) {
+        run_input_producer(p, c);
+        wait_drain(c.bar(kBarWLoad), 0, p.status);
+      }
+      __syncwarp();
+    } else if (warp >= kEpiWarp0) {
+      run_epilogue<V>(p, c, warp - kEpiWarp0, lane);
+    }
   }
 
   tc_fence_before_sync();
@@ -915,8 +1233,11 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
   p.d0 = dims[0];
   p.dL = dims[L];
   p.nslab_bits = 0;
-  for (int l = 0; l < L; ++l)
+  p.n16_bits = 0;
+  for (int l = 0; l < L; ++l) {
     p.nslab_bits |= static_cast<uint64_t>((dims[l] >> 4) - 1) << (4 * l);
+    p.n16_bits |= static_cast<uint64_t>((dims[l + 1] >> 4) - 1) << (4 * l);
+  }
   const uint32_t acc_cols = (nmax + 31u) & ~31u;  // widest layer, a multiple of 32
   // output staging: 8 KB per 32-column chunk, 4 KB for a trailing 16-column one
   p.out_slot_bytes = static_cast<uint32_t>(p.dL >> 5) * (kTileM * 64u) +
@@ -979,7 +1300,8 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
               p.ones_col = slots * p.slot_cols;
               p.n_slots = slots;
               p.n_groups = groups;
-              p.n_threads = 32u * (4u * slots * groups + (streamed ? 2u : 1u));
+              p.n_threads = streamed ? 32u * (4u * slots * groups + 2u)
+                                     : 32u * (static_cast<uint32_t>(kEpiWarp0) + 4u * slots * groups);
               p.in_stage_bytes = stage;
               p.n_in_stages = depth;
               p.n_out_bufs = obufs;

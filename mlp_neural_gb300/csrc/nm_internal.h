@@ -15,9 +15,13 @@ namespace nm {
 constexpr int kMaxSlots = 5;       // 128-sample tiles in flight per CTA (upper bound)
 constexpr int kMaxInStages = 2 * kMaxSlots;  // input TMA ring: up to 2 stages per slot
 constexpr int kMaxBStages = kMaxSlots;       // row-major ablation: one B stage per slot
-// Resident weights: each slot's warps (4 TMEM lane quadrants x column groups)
-// run its epilogue and issue its MMAs; then one input-producer warp.
-constexpr int kMaxSlotWarps = 4 * kMaxSlots > 16 ? 4 * kMaxSlots : 16;
+// Resident weights: warps 0 .. S-1 issue the slots' MMA chains (one warp per
+// tile slot), warp S produces the input tiles, and from warp kEpiWarp0 on
+// each slot has 4G epilogue warps (4 TMEM lane quadrants x G column groups);
+// warps between the producer and kEpiWarp0 have no role.
+constexpr int kEpiWarp0 = 8;
+constexpr int kMaxEpiWarps = 4 * kMaxSlots > 16 ? 4 * kMaxSlots : 16;
+constexpr int kMaxResidentWarps = kEpiWarp0 + kMaxEpiWarps;
 // Streamed weights: the slots' warps (16), one weight-producer warp and one
 // input-producer warp.
 constexpr int kStreamSlots = 2;    // tile slots at most with streamed weights
@@ -111,6 +115,7 @@ struct FusedParams {  // 128-byte aligned through its CUtensorMap members
   uint32_t sched_bytes;   // bytes of the schedule to copy
   uint32_t bslab_bytes;   // bytes of the bias-slab region
   uint64_t nslab_bits;    // 4 bits per layer: K_l / 16 - 1
+  uint64_t n16_bits;      // 4 bits per layer: N_l / 16 - 1
   uint32_t bias_row0[kMaxLayers];  // index of b_l[0] among the concatenated biases
   uint32_t bslab_off[kMaxLayers];  // byte offset of b_l's slab in the bias-slab region
   // shared-memory plan (byte offsets from the 1024-aligned base)

@@ -20,9 +20,16 @@ def nmlib():
 def test_benchmark_network_plans(nmlib, name, slots, warps, streamed):
     p = nmlib.plan(synth.WORKLOADS[name].dims)
     assert (p["tile_slots"], p["warps_per_slot"], p["streamed_weights"]) == (slots, warps, streamed)
-    assert p["threads"] == 32 * (slots * warps + 1 + streamed)
+    assert p["threads"] == _threads(slots, warps, streamed)
     assert p["weight_stages"] == (4 if streamed else 0)
     assert p["smem_bytes"] <= nmlib.GB300_SMEM_OPTIN and p["tmem_columns"] == 512
+
+
+def _threads(slots, warps, streamed):
+    # streamed weights: the slots' warps, a weight producer and an input
+    # producer; resident weights: eight warps for the slots' issuing warps
+    # and the input producer, then the slots' epilogue warps
+    return 32 * (slots * warps + 2) if streamed else 32 * (8 + slots * warps)
 
 
 def _tmem_needed(dims, slots):
@@ -50,7 +57,7 @@ def test_plan_invariants_over_random_networks(nmlib, variant):
         planned += 1
         slots, warps = p["tile_slots"], p["warps_per_slot"]
         assert 1 <= slots <= 5 and warps % 4 == 0
-        assert p["threads"] == 32 * (slots * warps + 1 + p["streamed_weights"]) <= 1024
+        assert p["threads"] == _threads(slots, warps, p["streamed_weights"]) <= 1024
         assert p["smem_bytes"] <= nmlib.GB300_SMEM_OPTIN
         t = p["tmem_columns"]
         assert 32 <= t <= 512 and t & (t - 1) == 0
