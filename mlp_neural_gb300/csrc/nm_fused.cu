@@ -206,93 +206,126 @@ __device__ __forceinline__ void convert_pairs(const uint32_t* acc, __half2 slope
   }
 }
 
-// One layer's k-slab MMAs as a straight-line sequence: the NS descriptor
-// pairs are loaded from the shared schedule table together (one load latency
-// instead of one per MMA) -- before `wait` runs, since the table is constant --
-// then, once `wait` has succeeded, the NS tcgen05.mma follow back to back with
-// no branch between them. A single thread issues MMAs only about one per
-// 60 cycles and a dependent load or a branch before each adds to that, so
-// the chain is the slot's critical path. Returns false if `wait` gave up.
-template <int NS, class Wait>
-__device__ __forceinline__ bool mma_seq_ss(uint32_t d, uint32_t tab, uint64_t a_add, uint64_t b_add,
-                                           uint32_t idesc, Wait&& wait) {
-  // Up to 8 descriptor pairs are fetched before the wait (register budget);
-  // the rest, together, right after it.
-  constexpr int kPre = NS < 8 ? NS : 8;
-  uint4 sd[NS];
-#pragma unroll
-  for (int k = 0; k < kPre; ++k) sd[k] = ld_shared_u32x4_ordered(tab + 16u * k);
-  if (!wait()) return false;
-#pragma unroll
-  for (int k = kPre; k < NS; ++k) sd[k] = ld_shared_u32x4_ordered(tab + 16u * k);
-  tc_fence_after_sync();
-#pragma unroll
-  for (int k = 0; k < NS; ++k)
-    umma_f16_ss(d, (static_cast<uint64_t>(sd[k].y) << 32 | sd[k].x) + a_add,
-                (static_cast<uint64_t>(sd[k].w) << 32 | sd[k].z) + b_add, idesc, k);
-  return true;
-}
-
-
-// Same with A in TMEM (resident-weight layout: k-slab k of the activations
-// starts 8 columns, 16 FP16 values per row, after slab k - 1); only the B
-// descriptors are needed. The first four of them arrive already loaded
-// (`pre`, fetched before the slot's barrier, off the critical path); the rest
-// are fetched here.
+// A layer's k-slab MMAs are issued in groups of up to four, each group a
+// straight-line sequence with its descriptors already in registers: a
+// branch or a dependent load between two MMAs costs the issuing thread far
+// more than the MMA itself, and the chain is the slot's critical path. The
+// groups keep the code small -- one four-way choice per group instead of a
+// fully unrolled sequence per slab count -- which matters because warps that
+// sleep at a barrier while others run must find their code still cached.
+// Descriptor rows k0 .. k0 + 3 of a layer always lie inside its 16-row block
+// of the schedule table, so a group may load all four.
 struct PreDesc {
   uint2 b0, b1, b2, b3;
 };
 
-template <int NS, bool kPre = true>
-__device__ __forceinline__ void mma_seq_ts(uint32_t d, uint32_t a_tmem, uint32_t tab, PreDesc pre,
-                                           uint64_t b_add, uint32_t idesc) {
-  uint2 bd[NS];
-#pragma unroll
-  for (int k = 0; k < NS; ++k)
-    bd[k] = (kPre && k == 0) ? pre.b0
-          : (kPre && k == 1) ? pre.b1
-          : (kPre && k == 2) ? pre.b2
-          : (kPre && k == 3) ? pre.b3
-                             : ld_shared_u32x2_ordered(tab + 16u * k + 8u);
-#pragma unroll
-  for (int k = 0; k < NS; ++k)
-    umma_f16_ts(d, a_tmem + 8u * k, (static_cast<uint64_t>(bd[k].y) << 32 | bd[k].x) + b_add, idesc,
-                k);
+__device__ __forceinline__ uint64_t desc_of(uint2 v) {
+  return static_cast<uint64_t>(v.y) << 32 | v.x;
 }
 
-// nslab = K / 16 is 1..16 (K <= 256); one switch picks the unrolled sequence.
-#define NM_SLAB_COUNTS(X) \
-  X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13) X(14) X(15) X(16)
+// B descriptors of slabs k0 .. k0 + 3 (A in TMEM needs no A descriptor).
+__device__ __forceinline__ PreDesc load_b4(uint32_t tab, uint32_t k0) {
+  const uint32_t a = tab + 16u * k0 + 8u;
+  PreDesc d;
+  d.b0 = ld_shared_u32x2_ordered(a);
+  d.b1 = ld_shared_u32x2_ordered(a + 16u);
+  d.b2 = ld_shared_u32x2_ordered(a + 32u);
+  d.b3 = ld_shared_u32x2_ordered(a + 48u);
+  return d;
+}
 
+// A in TMEM (resident-weight layout: slab k of the activations starts 8
+// columns, 16 FP16 values per row, after slab k - 1). N MMAs, slabs k0 ...
+template <int N>
+__device__ __forceinline__ void seq_ts(uint32_t d, uint32_t a_tmem, uint32_t k0, const PreDesc& b,
+                                       uint64_t b_add, uint32_t idesc) {
+  const uint32_t a = a_tmem + 8u * k0;
+  umma_f16_ts(d, a, desc_of(b.b0) + b_add, idesc, k0);
+  if (N > 1) umma_f16_ts(d, a + 8u, desc_of(b.b1) + b_add, idesc, 1u);
+  if (N > 2) umma_f16_ts(d, a + 16u, desc_of(b.b2) + b_add, idesc, 1u);
+  if (N > 3) umma_f16_ts(d, a + 24u, desc_of(b.b3) + b_add, idesc, 1u);
+}
+
+__device__ __forceinline__ void group_ts(uint32_t n, uint32_t d, uint32_t a_tmem, uint32_t k0,
+                                         const PreDesc& b, uint64_t b_add, uint32_t idesc) {
+  switch (n) {
+    case 1: seq_ts<1>(d, a_tmem, k0, b, b_add, idesc); break;
+    case 2: seq_ts<2>(d, a_tmem, k0, b, b_add, idesc); break;
+    case 3: seq_ts<3>(d, a_tmem, k0, b, b_add, idesc); break;
+    default: seq_ts<4>(d, a_tmem, k0, b, b_add, idesc); break;
+  }
+}
+
+// The whole chain on A in TMEM; the first group's descriptors arrive in
+// `pre` (fetched before the slot's barrier, off the critical path).
+__device__ __forceinline__ void mma_chain_ts(uint32_t nslab, uint32_t d, uint32_t a_tmem,
+                                             uint32_t tab, const PreDesc& pre, uint64_t b_add,
+                                             uint32_t idesc) {
+  group_ts(nslab < 4u ? nslab : 4u, d, a_tmem, 0u, pre, b_add, idesc);
+  for (uint32_t k0 = 4; k0 < nslab; k0 += 4) {
+    const PreDesc b = load_b4(tab, k0);
+    group_ts(nslab - k0 < 4u ? nslab - k0 : 4u, d, a_tmem, k0, b, b_add, idesc);
+  }
+}
+
+// A in shared memory (layer 1: the input tile): A and B descriptors of
+// slabs k0 .. k0 + 3.
+struct PreDesc2 {
+  uint4 s0, s1, s2, s3;
+};
+
+__device__ __forceinline__ PreDesc2 load_ab4(uint32_t tab, uint32_t k0) {
+  const uint32_t a = tab + 16u * k0;
+  PreDesc2 d;
+  d.s0 = ld_shared_u32x4_ordered(a);
+  d.s1 = ld_shared_u32x4_ordered(a + 16u);
+  d.s2 = ld_shared_u32x4_ordered(a + 32u);
+  d.s3 = ld_shared_u32x4_ordered(a + 48u);
+  return d;
+}
+
+template <int N>
+__device__ __forceinline__ void seq_ss(uint32_t d, uint32_t k0, const PreDesc2& s, uint64_t a_add,
+                                       uint64_t b_add, uint32_t idesc) {
+  umma_f16_ss(d, (static_cast<uint64_t>(s.s0.y) << 32 | s.s0.x) + a_add,
+              (static_cast<uint64_t>(s.s0.w) << 32 | s.s0.z) + b_add, idesc, k0);
+  if (N > 1)
+    umma_f16_ss(d, (static_cast<uint64_t>(s.s1.y) << 32 | s.s1.x) + a_add,
+                (static_cast<uint64_t>(s.s1.w) << 32 | s.s1.z) + b_add, idesc, 1u);
+  if (N > 2)
+    umma_f16_ss(d, (static_cast<uint64_t>(s.s2.y) << 32 | s.s2.x) + a_add,
+                (static_cast<uint64_t>(s.s2.w) << 32 | s.s2.z) + b_add, idesc, 1u);
+  if (N > 3)
+    umma_f16_ss(d, (static_cast<uint64_t>(s.s3.y) << 32 | s.s3.x) + a_add,
+                (static_cast<uint64_t>(s.s3.w) << 32 | s.s3.z) + b_add, idesc, 1u);
+}
+
+__device__ __forceinline__ void group_ss(uint32_t n, uint32_t d, uint32_t k0, const PreDesc2& s,
+                                         uint64_t a_add, uint64_t b_add, uint32_t idesc) {
+  switch (n) {
+    case 1: seq_ss<1>(d, k0, s, a_add, b_add, idesc); break;
+    case 2: seq_ss<2>(d, k0, s, a_add, b_add, idesc); break;
+    case 3: seq_ss<3>(d, k0, s, a_add, b_add, idesc); break;
+    default: seq_ss<4>(d, k0, s, a_add, b_add, idesc); break;
+  }
+}
+
+// The chain on the input tile: the first group's descriptors are loaded
+// before `wait` (the input tile's arrival) runs, since the table is
+// constant. Returns false if `wait` gave up.
 template <class Wait>
 __device__ __forceinline__ bool mma_chain_ss(uint32_t nslab, uint32_t d, uint32_t tab,
                                              uint64_t a_add, uint64_t b_add, uint32_t idesc,
                                              Wait&& wait) {
-  switch (nslab) {
-#define NM_CASE(n) \
-  case n:          \
-    return mma_seq_ss<n>(d, tab, a_add, b_add, idesc, wait);
-    NM_SLAB_COUNTS(NM_CASE)
-#undef NM_CASE
-    default:
-      return false;
+  const PreDesc2 first = load_ab4(tab, 0u);
+  if (!wait()) return false;
+  tc_fence_after_sync();
+  group_ss(nslab < 4u ? nslab : 4u, d, 0u, first, a_add, b_add, idesc);
+  for (uint32_t k0 = 4; k0 < nslab; k0 += 4) {
+    const PreDesc2 s = load_ab4(tab, k0);
+    group_ss(nslab - k0 < 4u ? nslab - k0 : 4u, d, k0, s, a_add, b_add, idesc);
   }
-}
-
-template <bool kPre = true>
-__device__ __forceinline__ void mma_chain_ts(uint32_t nslab, uint32_t d, uint32_t a_tmem,
-                                             uint32_t tab, PreDesc pre, uint64_t b_add,
-                                             uint32_t idesc) {
-  switch (nslab) {
-#define NM_CASE(n) \
-  case n:          \
-    mma_seq_ts<n, kPre>(d, a_tmem, tab, pre, b_add, idesc); \
-    break;
-    NM_SLAB_COUNTS(NM_CASE)
-#undef NM_CASE
-    default:
-      break;
-  }
+  return true;
 }
 
 __device__ __forceinline__ void issue_input_tma(const FusedParams& p, uint32_t dst, uint32_t bar,
@@ -551,7 +584,7 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
       ok = mma_chain_ss(nslab, slot_tmem, tab, a_add, b_add, li.idesc, wait);
     } else {
       tc_fence_after_sync();
-      mma_chain_ts<false>(nslab, slot_tmem, slot_tmem + p.a_col, tab, PreDesc{}, b_add, li.idesc);
+      mma_chain_ts(nslab, slot_tmem, slot_tmem + p.a_col, tab, load_b4(tab, 0u), b_add, li.idesc);
     }
     if (ok) {
       umma_f16_ts(slot_tmem, c.tmem + p.ones_col, bias_bd, li.idesc, 1u);
@@ -767,12 +800,7 @@ __device__ __forceinline__ void run_issuer(const FusedParams& p, const Ctx& c, i
     ip.bias_bd = smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u);
     ip.nslab = static_cast<uint32_t>((p.nslab_bits >> (4 * l)) & 15u) + 1u;
     ip.tab = c.slab_addr(p, 16u * static_cast<uint32_t>(l));
-    // Rows past the layer's last slab still lie inside the table (16 rows
-    // per layer), so this fixed-count prefetch stays in bounds.
-    ip.bd.b0 = ld_shared_u32x2_ordered(ip.tab + 8u);
-    ip.bd.b1 = ld_shared_u32x2_ordered(ip.tab + 24u);
-    ip.bd.b2 = ld_shared_u32x2_ordered(ip.tab + 40u);
-    ip.bd.b3 = ld_shared_u32x2_ordered(ip.tab + 56u);
+    ip.bd = load_b4(ip.tab, 0u);
     return ip;
   };
   auto fire_ts = [&](const IssuePrep& ip) {
