@@ -787,6 +787,8 @@ __device__ __forceinline__ void run_issuer(const FusedParams& p, const Ctx& c, i
 
   // Everything a chain on A in TMEM needs that does not depend on the
   // epilogue: the layer's entry and its first B descriptors.
+  // The first group's B descriptors are complete (base added) in `bd`, so
+  // that after the barrier only the MMAs and the commit remain.
   struct IssuePrep {
     uint64_t b_add, bias_bd;
     uint32_t idesc, nslab, tab;
@@ -801,11 +803,25 @@ __device__ __forceinline__ void run_issuer(const FusedParams& p, const Ctx& c, i
     ip.nslab = static_cast<uint32_t>((p.nslab_bits >> (4 * l)) & 15u) + 1u;
     ip.tab = c.slab_addr(p, 16u * static_cast<uint32_t>(l));
     ip.bd = load_b4(ip.tab, 0u);
+    auto add = [&](uint2& v) {
+      const uint64_t d = desc_of(v) + ip.b_add;
+      v.x = static_cast<uint32_t>(d);
+      v.y = static_cast<uint32_t>(d >> 32);
+    };
+    add(ip.bd.b0);
+    add(ip.bd.b1);
+    add(ip.bd.b2);
+    add(ip.bd.b3);
     return ip;
   };
   auto fire_ts = [&](const IssuePrep& ip) {
     tc_fence_after_sync();
-    mma_chain_ts(ip.nslab, slot_tmem, slot_tmem + p.a_col, ip.tab, ip.bd, ip.b_add, ip.idesc);
+    const uint32_t a = slot_tmem + p.a_col;
+    group_ts(ip.nslab < 4u ? ip.nslab : 4u, slot_tmem, a, 0u, ip.bd, 0u, ip.idesc);
+    for (uint32_t k0 = 4; k0 < ip.nslab; k0 += 4) {
+      const PreDesc b = load_b4(ip.tab, k0);
+      group_ts(ip.nslab - k0 < 4u ? ip.nslab - k0 : 4u, slot_tmem, a, k0, b, ip.b_add, ip.idesc);
+    }
     umma_f16_ts(slot_tmem, c.tmem + p.ones_col, ip.bias_bd, ip.idesc, 1u);
     umma_commit(c.bar(kBarAccFull + s));
   };
@@ -847,9 +863,8 @@ __device__ __forceinline__ void run_issuer(const FusedParams& p, const Ctx& c, i
             if (elect_one()) iok = issue_first(r);
             ok = __all_sync(0xFFFFFFFFu, iok);
           }
-        } else {
-          if (ok && elect_one()) fire_ts(ip);
-          __syncwarp();
+        } else if (ok && elect_one()) {
+          fire_ts(ip);
         }
         // ... then, while its epilogue runs, the next chain's descriptors
         // (layers after the first), and the barrier after that epilogue.
