@@ -31,7 +31,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 CLOCK_FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-VARIANTS = {"fused": 0, "rowmajor": 1, "scalar": 2}
+VARIANTS = {"fused": 0, "rowmajor": 1, "scalar": 2, "paired": 3}
 
 
 def parse_args(argv=None):

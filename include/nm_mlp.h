@@ -85,7 +85,14 @@ typedef enum nm_variant {
     /* Ablation of the activation: the epilogue walks the FP16 values one by
      * one with a dynamic index and a branch, if (h < 0) h *= half(0.01)
      * ("Bad versus good activation", bad form). */
-    NM_VARIANT_SCALAR_ACTIVATION = 2
+    NM_VARIANT_SCALAR_ACTIVATION = 2,
+    /* The fused kernel with two tile regions (256 samples) per issuing warp:
+     * one warp issues both tiles' MMA chains of a layer and meets both
+     * tiles' epilogue warps at one barrier (five regions are issued as
+     * 2 + 2 + 1). A larger M per issue than the default one tile per
+     * issuing warp; measured slower on the benchmark networks, kept as a
+     * measured alternative. Same arithmetic, bit-identical outputs. */
+    NM_VARIANT_PAIRED_TILES = 3
 } nm_variant;
 
 /* Version of this ABI (bumped on any incompatible change). */
@@ -254,6 +261,8 @@ typedef struct nm_plan {
   int32_t output_buffers;   /* output staging buffers per slot */
   uint32_t smem_bytes;      /* dynamic shared memory per CTA */
   uint32_t tmem_columns;    /* tensor memory columns allocated per CTA */
+  int32_t issuing_warps;    /* warps that issue MMA chains (one per slot, or per pair of
+                               slots with NM_VARIANT_PAIRED_TILES) */
 } nm_plan;
 
 nm_status nm_mlp_plan(const int32_t *dims, int32_t n_dims, nm_variant variant,

@@ -373,7 +373,7 @@ nm_status ensure_host_pipeline(nm_mlp* h) {
 
 extern "C" {
 
-int32_t nm_abi_version(void) { return 1; }
+int32_t nm_abi_version(void) { return 2; }
 
 const char* nm_status_str(nm_status s) {
   switch (s) {
@@ -392,7 +392,7 @@ nm_status nm_mlp_plan(const int32_t* dims, int32_t n_dims, nm_variant variant,
                       uint32_t smem_optin, nm_plan* plan) {
   if (!plan) return NM_ERR_INVALID_ARG;
   if (variant != NM_VARIANT_FUSED && variant != NM_VARIANT_ROWMAJOR_WEIGHTS &&
-      variant != NM_VARIANT_SCALAR_ACTIVATION)
+      variant != NM_VARIANT_SCALAR_ACTIVATION && variant != NM_VARIANT_PAIRED_TILES)
     return NM_ERR_INVALID_ARG;
   const nm_status dst = nm::check_dims(dims, n_dims);
   if (dst != NM_OK) return dst;
@@ -417,6 +417,8 @@ nm_status nm_mlp_plan(const int32_t* dims, int32_t n_dims, nm_variant variant,
   plan->output_buffers = static_cast<int32_t>(p.n_out_bufs);
   plan->smem_bytes = smem;
   plan->tmem_columns = p.tmem_cols;
+  plan->issuing_warps = p.stream_w ? static_cast<int32_t>(p.n_slots)
+                                   : static_cast<int32_t>(p.n_groups_issue);
   return NM_OK;
 }
 
@@ -601,7 +603,8 @@ nm_status nm_mlp_set_host_chunk(nm_mlp* h, int64_t rows) {
 
 nm_status nm_mlp_set_variant(nm_mlp* h, nm_variant v) {
   if (!h) return NM_ERR_INVALID_ARG;
-  if (v != NM_VARIANT_FUSED && v != NM_VARIANT_ROWMAJOR_WEIGHTS && v != NM_VARIANT_SCALAR_ACTIVATION)
+  if (v != NM_VARIANT_FUSED && v != NM_VARIANT_ROWMAJOR_WEIGHTS && v != NM_VARIANT_SCALAR_ACTIVATION &&
+      v != NM_VARIANT_PAIRED_TILES)
     return NM_ERR_INVALID_ARG;
   h->variant = static_cast<int>(v);
   return NM_OK;

@@ -695,7 +695,7 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
             st_shared_v4_nc(base + swz(row * 32u + cc * 16u, 16), h[4 * cc], h[4 * cc + 1],
                             h[4 * cc + 2], h[4 * cc + 3]);
         }
-        if (V == kVarRowMajor && r + 1 < n_rounds) rebuild_b(0);
+        if (V == kVarRowMajor && (r + 1) * S + s < c.n_local) rebuild_b(0);
         fence_proxy_async_smem();  // staging tile -> TMA store (async proxy)
       }
       tc_fence_before_sync();
@@ -775,20 +775,25 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
 // landed; later layers read A from TMEM, and their descriptors are fetched
 // before the barrier.
 template <int V>
-__device__ __forceinline__ void run_issuer(const FusedParams& p, const Ctx& c, int32_t s, int lane) {
+__device__ __forceinline__ void run_issuer(const FusedParams& p, const Ctx& c, int32_t g, int lane) {
   const int32_t S = static_cast<int32_t>(p.n_slots);
   const int L = p.L;
   const uint32_t D = p.n_in_stages;
-  const int32_t n_rounds = (c.n_local - s + S - 1) / S;
-  const uint32_t slot_tmem = c.tmem + static_cast<uint32_t>(s) * p.slot_cols;
-  const uint32_t bar_id = 1u + static_cast<uint32_t>(s);
-  const uint32_t bar_threads = 32u * (4u * p.n_groups + 1u);
-  const uint32_t b_stage = c.sbase + p.sm_b + static_cast<uint32_t>(s) * p.b_stage_bytes;
+  const int32_t s0 = static_cast<int32_t>(p.grp_first[g]);  // the group's first tile region
+  const int32_t T = static_cast<int32_t>(p.grp_tiles[g]);   // its regions (1 or 2)
+  const int32_t n_rounds = (c.n_local - s0 + S - 1) / S;    // rounds with a tile in region s0
+  const uint32_t bar_id = 1u + static_cast<uint32_t>(g);
+  const uint32_t bar_threads = 32u * (4u * p.n_groups * static_cast<uint32_t>(T) + 1u);
+  auto tmem_of = [&](int32_t s) { return c.tmem + static_cast<uint32_t>(s) * p.slot_cols; };
+  auto b_stage_of = [&](int32_t s) {
+    return c.sbase + p.sm_b + static_cast<uint32_t>(s) * p.b_stage_bytes;
+  };
 
   // Everything a chain on A in TMEM needs that does not depend on the
-  // epilogue: the layer's entry and its first B descriptors.
-  // The first group's B descriptors are complete (base added) in `bd`, so
-  // that after the barrier only the MMAs and the commit remain.
+  // epilogue -- the layer's entry and its first B descriptors -- shared by
+  // the group's regions (same layer, same weights). The first group's B
+  // descriptors are complete (base added), so that after the barrier only
+  // the MMAs and the commits remain.
   struct IssuePrep {
     uint64_t b_add, bias_bd;
     uint32_t idesc, nslab, tab;
@@ -798,7 +803,7 @@ __device__ __forceinline__ void run_issuer(const FusedParams& p, const Ctx& c, i
     IssuePrep ip;
     const LayerRegs li = load_layer(p, c, l);
     ip.idesc = li.idesc;
-    ip.b_add = ((V == kVarRowMajor) ? b_stage : c.sbase + p.sm_w + li.w_off) >> 4;
+    ip.b_add = ((V == kVarRowMajor) ? b_stage_of(s0) : c.sbase + p.sm_w + li.w_off) >> 4;
     ip.bias_bd = smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u);
     ip.nslab = static_cast<uint32_t>((p.nslab_bits >> (4 * l)) & 15u) + 1u;
     ip.tab = c.slab_addr(p, 16u * static_cast<uint32_t>(l));
@@ -814,32 +819,51 @@ __device__ __forceinline__ void run_issuer(const FusedParams& p, const Ctx& c, i
     add(ip.bd.b3);
     return ip;
   };
-  auto fire_ts = [&](const IssuePrep& ip) {
-    tc_fence_after_sync();
-    const uint32_t a = slot_tmem + p.a_col;
-    group_ts(ip.nslab < 4u ? ip.nslab : 4u, slot_tmem, a, 0u, ip.bd, 0u, ip.idesc);
+  // Chain of region s (A in TMEM). In the row-major ablation each region
+  // has its own B stage, so the second region's descriptors are rebased.
+  auto fire_ts = [&](const IssuePrep& ip, int32_t s) {
+    const uint32_t d = tmem_of(s);
+    const uint32_t a = d + p.a_col;
+    uint64_t b_add = ip.b_add;
+    PreDesc bd = ip.bd;
+    if (V == kVarRowMajor && s != s0) {
+      const uint64_t delta = static_cast<uint64_t>((b_stage_of(s) - b_stage_of(s0)) >> 4);
+      b_add += delta;
+      auto add = [&](uint2& v) {
+        const uint64_t x = desc_of(v) + delta;
+        v.x = static_cast<uint32_t>(x);
+        v.y = static_cast<uint32_t>(x >> 32);
+      };
+      add(bd.b0);
+      add(bd.b1);
+      add(bd.b2);
+      add(bd.b3);
+    }
+    group_ts(ip.nslab < 4u ? ip.nslab : 4u, d, a, 0u, bd, 0u, ip.idesc);
     for (uint32_t k0 = 4; k0 < ip.nslab; k0 += 4) {
       const PreDesc b = load_b4(ip.tab, k0);
-      group_ts(ip.nslab - k0 < 4u ? ip.nslab - k0 : 4u, slot_tmem, a, k0, b, ip.b_add, ip.idesc);
+      group_ts(ip.nslab - k0 < 4u ? ip.nslab - k0 : 4u, d, a, k0, b, b_add, ip.idesc);
     }
-    umma_f16_ts(slot_tmem, c.tmem + p.ones_col, ip.bias_bd, ip.idesc, 1u);
+    umma_f16_ts(d, c.tmem + p.ones_col, ip.bias_bd, ip.idesc, 1u);
     umma_commit(c.bar(kBarAccFull + s));
   };
-  // Layer 1 of round rr: A is the input tile in the slot's ring stage.
-  auto issue_first = [&](int32_t rr) -> bool {
+  // Layer 1 of round rr in region s: A is the input tile in the region's
+  // ring stage.
+  auto issue_first = [&](int32_t rr, int32_t s) -> bool {
     const LayerRegs li = load_layer(p, c, 0);
     const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(rr) % D;
-    const uint32_t b_base = (V == kVarRowMajor) ? b_stage : c.sbase + p.sm_w + li.w_off;
+    const uint32_t b_base = (V == kVarRowMajor) ? b_stage_of(s) : c.sbase + p.sm_w + li.w_off;
     const uint32_t nslab = static_cast<uint32_t>(p.nslab_bits & 15u) + 1u;
     const uint64_t a_add = (c.sbase + p.sm_in + st * p.in_stage_bytes) >> 4;
     auto wait = [&]() -> bool {
       return wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(rr) / D) & 1u, p.wait_ns,
                         c.abort_flag, p.status);
     };
-    if (!mma_chain_ss(nslab, slot_tmem, c.slab_addr(p, 0u), a_add, b_base >> 4, li.idesc, wait))
+    const uint32_t d = tmem_of(s);
+    if (!mma_chain_ss(nslab, d, c.slab_addr(p, 0u), a_add, b_base >> 4, li.idesc, wait))
       return false;
-    umma_f16_ts(slot_tmem, c.tmem + p.ones_col,
-                smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u), li.idesc, 1u);
+    umma_f16_ts(d, c.tmem + p.ones_col, smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u),
+                li.idesc, 1u);
     umma_commit(c.bar(kBarAccFull + s));
     umma_commit(c.bar(kBarInEmpty + st));
     return true;
@@ -855,18 +879,24 @@ __device__ __forceinline__ void run_issuer(const FusedParams& p, const Ctx& c, i
     named_bar_sync(bar_id, bar_threads);  // the epilogue warps are set up
     IssuePrep ip;
     for (int32_t r = 0; r < n_rounds; ++r) {
+      // the group's regions that hold a tile this round (the last round may
+      // be partial)
+      const int32_t nt = (r * S + s0 + T <= c.n_local) ? T : c.n_local - (r * S + s0);
       for (int l = 0; l < L; ++l) {
-        // Chain (r, l) ...
+        // Chain (r, l) of each of the group's tiles ...
         if (l == 0) {
           if (ok) {
             bool iok = true;
-            if (elect_one()) iok = issue_first(r);
+            if (elect_one()) {
+              for (int32_t t = 0; t < nt && iok; ++t) iok = issue_first(r, s0 + t);
+            }
             ok = __all_sync(0xFFFFFFFFu, iok);
           }
         } else if (ok && elect_one()) {
-          fire_ts(ip);
+          fire_ts(ip, s0);
+          if (nt > 1) fire_ts(ip, s0 + 1);
         }
-        // ... then, while its epilogue runs, the next chain's descriptors
+        // ... then, while their epilogue runs, the next chain's descriptors
         // (layers after the first), and the barrier after that epilogue.
         if (l + 1 < L) ip = prep_ts(l + 1);
         tc_fence_before_sync();
@@ -877,8 +907,8 @@ __device__ __forceinline__ void run_issuer(const FusedParams& p, const Ctx& c, i
   // Drain: every MMA this warp issued completes before the CTA may exit (the
   // lane elect.sync picks here is the one that issued them).
   if (elect_one()) {
-    umma_commit(c.bar(kBarDrain + s));
-    wait_drain(c.bar(kBarDrain + s), 0, p.status);
+    umma_commit(c.bar(kBarDrain + g));
+    wait_drain(c.bar(kBarDrain + g), 0, p.status);
   }
   __syncwarp();
 }
@@ -902,12 +932,16 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
   const uint32_t lane_bits = static_cast<uint32_t>(quad * 32) << 16;
   const uint32_t tbase = c.tmem + static_cast<uint32_t>(s) * p.slot_cols + lane_bits;
   const uint32_t a_tmem = tbase + p.a_col;
-  const uint32_t bar_id = 1u + static_cast<uint32_t>(s);
-  const uint32_t bar_threads = 32u * static_cast<uint32_t>(nw + 1);
+  const uint32_t grp = p.grp_of[s];
+  const int32_t s0 = static_cast<int32_t>(p.grp_first[grp]);
+  const uint32_t bar_id = 1u + grp;
+  const uint32_t bar_threads = 32u * static_cast<uint32_t>(nw) * p.grp_tiles[grp] + 32u;
   const __half2 slope2 = __float2half2_rn(0.01f);  // half(0.01)
   const int L = p.L;
   const int n_out = p.dL;
-  const int32_t n_rounds = (c.n_local - s + S - 1) / S;  // tiles r*S + s < n_local
+  // The group's rounds (those of its first region); this region holds a tile
+  // in all of them but possibly the last.
+  const int32_t n_rounds = (c.n_local - s0 + S - 1) / S;
   const bool storer = (lane == 0) && (32 * g < n_out);
   const uint32_t b_stage = c.sbase + p.sm_b + static_cast<uint32_t>(s) * p.b_stage_bytes;
 
@@ -936,12 +970,13 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
   }
   for (int32_t r = 0; r < n_rounds; ++r) {
     const int32_t t = tile_of(r * S + s);
+    const bool has = r * S + s < c.n_local;  // else: pass the group's barriers only
     // Hidden layers: accumulator -> FP16 -> activation -> next layer's A.
     for (int l = 0; l < L - 1; ++l) {
       const uint32_t q = static_cast<uint32_t>(r * L + l);
       const int N = layer_n(p, l);
-      if (ok) ok = warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c);
-      if (ok) {
+      if (ok && has) ok = warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c);
+      if (ok && has) {
         tc_fence_after_sync();
         for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
           uint32_t acc[32], h[16];
@@ -982,8 +1017,8 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
           bulk_wait_group_read<0>();
       }
       __syncwarp();
-      if (ok) ok = warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c);
-      if (ok) {
+      if (ok && has) ok = warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c);
+      if (ok && has) {
         tc_fence_after_sync();
         for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
           uint32_t acc[32], h[16];
@@ -1008,12 +1043,12 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
             st_shared_v4_nc(base + swz(row * 32u + cc * 16u, 16), h[4 * cc], h[4 * cc + 1],
                             h[4 * cc + 2], h[4 * cc + 3]);
         }
-        if (V == kVarRowMajor && r + 1 < n_rounds) rebuild_b(0);
+        if (V == kVarRowMajor && (r + 1) * S + s < c.n_local) rebuild_b(0);
         fence_proxy_async_smem();  // staging tile -> TMA store (async proxy)
       }
       tc_fence_before_sync();
       named_bar_sync(bar_id, bar_threads);
-      if (storer && ok) {
+      if (storer && ok && has) {
         const int64_t row0 = static_cast<int64_t>(t) * kTileM + quad * 32;
         if (row0 < p.n) {
           for (int c0 = 32 * g; c0 < N; c0 += 32 * G) {
@@ -1201,7 +1236,7 @@ __global__ void __launch_bounds__(is_stream(V) ? 32 * (16 + 2) : 32 * kMaxReside
   } else {
     // Resident weights: the slots' issuing warps, the input producer, then
     // (from kEpiWarp0) the slots' epilogue warps.
-    const int S = static_cast<int>(p.n_slots);
+    const int S = static_cast<int>(p.n_groups_issue);
     if (warp < S) {
       run_issuer<V>(p, c, warp, lane);
     } else if (warp == S) {
@@ -1342,6 +1377,22 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
               p.tmem_cols = cols;
               p.ones_col = slots * p.slot_cols;
               p.n_slots = slots;
+              // Issue groups: one tile region each, or (paired-tiles variant,
+              // one column group per warp) pairs of regions while at least two
+              // are left.
+              {
+                const bool pair = variant == kVarPaired && !streamed && groups == 1;
+                uint32_t ng = 0;
+                for (uint32_t r0 = 0; r0 < slots;) {
+                  const uint32_t t = (pair && slots - r0 >= 2) ? 2u : 1u;
+                  p.grp_first[ng] = r0;
+                  p.grp_tiles[ng] = t;
+                  for (uint32_t k = 0; k < t; ++k) p.grp_of[r0 + k] = ng;
+                  r0 += t;
+                  ++ng;
+                }
+                p.n_groups_issue = ng;
+              }
               p.n_groups = groups;
               p.n_threads = streamed ? 32u * (4u * slots * groups + 2u)
                                      : 32u * (static_cast<uint32_t>(kEpiWarp0) + 4u * slots * groups);
@@ -1408,12 +1459,14 @@ static cudaError_t launch_variant(const FusedParams& p, int grid, uint32_t smem,
 cudaError_t launch_fused(const FusedParams& p, int variant, int grid, uint32_t smem,
                          cudaStream_t stream, bool overlap) {
   if (p.stream_w) {
-    if (variant == kVarFused) return launch_variant<kVarFusedStream>(p, grid, smem, stream, overlap);
+    if (variant == kVarFused || variant == kVarPaired)
+      return launch_variant<kVarFusedStream>(p, grid, smem, stream, overlap);
     if (variant == kVarScalar) return launch_variant<kVarScalarStream>(p, grid, smem, stream, overlap);
     return cudaErrorInvalidValue;
   }
   switch (variant) {
-    case kVarFused: return launch_variant<kVarFused>(p, grid, smem, stream, overlap);
+    case kVarFused:
+    case kVarPaired: return launch_variant<kVarFused>(p, grid, smem, stream, overlap);
     case kVarRowMajor: return launch_variant<kVarRowMajor>(p, grid, smem, stream, overlap);
     case kVarScalar: return launch_variant<kVarScalar>(p, grid, smem, stream, overlap);
     default: return cudaErrorInvalidValue;

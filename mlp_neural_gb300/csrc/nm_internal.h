@@ -29,15 +29,18 @@ constexpr int kOutBufs = 2;        // output staging buffers per slot (TMA-store
 constexpr int kMaxSlabs = kMaxLayers * (kMaxDim / 16);
 constexpr uint32_t kStatusTimeout = 1u;
 
-// Public variants 0..2 (nm_variant); 3 and 4 are the fused and the
+// Public variants 0..3 (nm_variant); 4 and 5 are the fused and the
 // scalar-activation kernels with streamed instead of resident weights, chosen
-// by the planner when the packed weights do not fit in shared memory.
+// by the planner when the packed weights do not fit in shared memory. The
+// paired-tiles variant runs the fused kernel with a plan that issues the tile
+// regions two at a time.
 enum Variant : int {
   kVarFused = 0,
   kVarRowMajor = 1,
   kVarScalar = 2,
-  kVarFusedStream = 3,
-  kVarScalarStream = 4
+  kVarPaired = 3,
+  kVarFusedStream = 4,
+  kVarScalarStream = 5
 };
 constexpr int kMaxWStages = 4;     // streamed-weight ring depth (upper bound)
 
@@ -123,7 +126,12 @@ struct FusedParams {  // 128-byte aligned through its CUtensorMap members
   uint32_t in_stage_bytes, out_slot_bytes, b_stage_bytes;
   uint32_t n_in_stages;  // input stages per slot
   uint32_t n_b_stages, n_out_bufs;
-  uint32_t n_slots;     // tiles in flight
+  uint32_t n_slots;     // tiles in flight (tile regions of TMEM)
+  // Resident weights: the tile regions are issued in groups of one or two
+  // regions, one issuing warp and one named barrier per group; group g
+  // covers regions grp_first[g] .. grp_first[g] + grp_tiles[g] - 1.
+  uint32_t n_groups_issue;
+  uint32_t grp_first[kMaxSlots], grp_tiles[kMaxSlots], grp_of[kMaxSlots];
   uint32_t n_groups;    // column groups of a slot's epilogue (4 * n_groups warps per slot)
   uint32_t n_threads;   // block size
   uint32_t tmem_cols;   // allocated TMEM columns (power of two)

@@ -23,6 +23,7 @@ NM_ERR_TIMEOUT = 6
 NM_VARIANT_FUSED = 0
 NM_VARIANT_ROWMAJOR_WEIGHTS = 1
 NM_VARIANT_SCALAR_ACTIVATION = 2
+NM_VARIANT_PAIRED_TILES = 3
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnmmlp.so")
 
@@ -109,7 +110,7 @@ class Plan(ctypes.Structure):
                 ("threads", ctypes.c_int32), ("streamed_weights", ctypes.c_int32),
                 ("weight_stages", ctypes.c_int32), ("input_stages", ctypes.c_int32),
                 ("output_buffers", ctypes.c_int32), ("smem_bytes", ctypes.c_uint32),
-                ("tmem_columns", ctypes.c_uint32)]
+                ("tmem_columns", ctypes.c_uint32), ("issuing_warps", ctypes.c_int32)]
 
 
 GB300_SMEM_OPTIN = 232448  # opt-in shared memory per block on GB300, bytes

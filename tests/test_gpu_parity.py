@@ -148,6 +148,17 @@ def test_ablation_variants_bit_identical(dims):
     assert np.array_equal(y0, y1) and np.array_equal(y0, y2)
 
 
+@pytest.mark.parametrize("dims", [synth.WORKLOADS["tiny"].dims, synth.WORKLOADS["page"].dims,
+                                  (48, 80, 112, 16), (64, 128, 128, 32)])
+@pytest.mark.parametrize("n", [5000, 152 * 128 * 6 + 333])
+def test_paired_tiles_variant_bit_identical(dims, n):
+    # two tile regions per issuing warp, including CTAs whose last round
+    # fills only part of a pair
+    W, b, x = synth.small_net_inputs(dims, seed=9, n=n)
+    m = make_net(dims, W, b)
+    assert np.array_equal(_run(m, x, variant=0), _run(m, x, variant=3))
+
+
 @pytest.mark.parametrize("dims", STREAMED_DIMS)
 def test_streamed_weights_scalar_activation_bit_identical(dims):
     W, b, x = synth.small_net_inputs(dims, seed=8, n=3000)

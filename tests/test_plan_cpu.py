@@ -42,7 +42,19 @@ def _tmem_needed(dims, slots):
     return slots * (acc + r32(hidden // 2)) + 32
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("name,fused_issuers,paired_issuers", [
+    ("tiny", 5, 3), ("page", 5, 3), ("wide", 2, 2), ("hetero", 1, 1)])
+def test_issuing_warps(nmlib, name, fused_issuers, paired_issuers):
+    # one issuing warp per tile slot; the paired-tiles variant issues the
+    # resident-weight slots two at a time (2 + 2 + 1 for five slots)
+    dims = synth.WORKLOADS[name].dims
+    assert nmlib.plan(dims)["issuing_warps"] == fused_issuers
+    p = nmlib.plan(dims, nmlib.NM_VARIANT_PAIRED_TILES)
+    assert p["issuing_warps"] == paired_issuers
+    assert p["tile_slots"] == nmlib.plan(dims)["tile_slots"]
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
 def test_plan_invariants_over_random_networks(nmlib, variant):
     rng = np.random.default_rng(100 + variant)
     planned = 0
@@ -65,8 +77,11 @@ def test_plan_invariants_over_random_networks(nmlib, variant):
         assert p["input_stages"] in (1, 2) and p["output_buffers"] in (1, 2)
         if p["streamed_weights"]:
             assert variant != 1 and slots <= 2 and 2 <= p["weight_stages"] <= 4
+            assert p["issuing_warps"] == slots
         else:
             assert p["weight_stages"] == 0
+            paired = variant == 3 and warps == 4
+            assert p["issuing_warps"] == ((slots + 1) // 2 if paired else slots)
     assert planned > 200
 
 
