@@ -72,8 +72,18 @@ def lib():
             L.or_pack.restype = ctypes.c_int
             L.or_unpack.argtypes = [P, ctypes.c_int32, P, P, P]
             L.or_unpack.restype = ctypes.c_int
+            L.or_mlp_forward_fp8.argtypes = [P, ctypes.c_int32, P, P, P, ctypes.c_int64, P]
+            L.or_mlp_forward_fp8.restype = ctypes.c_int
+            L.or_fp8_layout.argtypes = [P, ctypes.c_int32, P]
+            L.or_fp8_layout.restype = ctypes.c_int64
+            L.or_pack_fp8.argtypes = [P, ctypes.c_int32, P, P]
+            L.or_pack_fp8.restype = ctypes.c_int
+            L.or_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+            L.or_e4m3_to_f32.restype = f32
+            L.or_f16_to_e4m3.argtypes = [u16]
+            L.or_f16_to_e4m3.restype = ctypes.c_uint8
             for name in ("or_f16_to_f32_n", "or_f32_to_f16_n", "or_leaky_max_n",
-                         "or_leaky_branchy_n"):
+                         "or_leaky_branchy_n", "or_e4m3_to_f32_n", "or_f16_to_e4m3_n"):
                 getattr(L, name).argtypes = [P, ctypes.c_int64, P]
                 getattr(L, name).restype = None
             _lib = L
@@ -140,6 +150,20 @@ def leaky_branchy_array(h) -> np.ndarray:
     return out
 
 
+def e4m3_to_f32_array(c) -> np.ndarray:
+    c = np.ascontiguousarray(c, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float32)
+    lib().or_e4m3_to_f32_n(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def f16_to_e4m3_array(h) -> np.ndarray:
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    out = np.empty(h.shape, dtype=np.uint8)
+    lib().or_f16_to_e4m3_n(_ptr(h), h.size, _ptr(out))
+    return out
+
+
 def forward(dims, W, b, x) -> np.ndarray:
     """Evaluate the network on every row of ``x``.
 
@@ -147,6 +171,16 @@ def forward(dims, W, b, x) -> np.ndarray:
     shape [d_{l+1}, d_l]; ``b[l]`` has d_{l+1} entries; ``x`` is uint16
     [n, d_0]. Returns uint16 [n, d_L].
     """
+    return _forward(lib().or_mlp_forward, dims, W, b, x)
+
+
+def forward_fp8(dims, W, b, x) -> np.ndarray:
+    """The narrow-precision pass (E4M3 weights of layers 2..L and E4M3
+    activations feeding them), same arguments as ``forward``."""
+    return _forward(lib().or_mlp_forward_fp8, dims, W, b, x)
+
+
+def _forward(fn, dims, W, b, x) -> np.ndarray:
     dims = _dims_arr(dims)
     L = len(dims) - 1
     W = [np.ascontiguousarray(w, dtype=np.uint16) for w in W]
@@ -158,10 +192,9 @@ def forward(dims, W, b, x) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.uint16)
     assert x.ndim == 2 and x.shape[1] == dims[0]
     y = np.zeros((x.shape[0], dims[-1]), dtype=np.uint16)
-    rc = lib().or_mlp_forward(_ptr(dims), L, _ptr_array(W), _ptr_array(b),
-                              _ptr(x), x.shape[0], _ptr(y))
+    rc = fn(_ptr(dims), L, _ptr_array(W), _ptr_array(b), _ptr(x), x.shape[0], _ptr(y))
     if rc != 0:
-        raise ValueError(f"or_mlp_forward rejected dims {dims.tolist()} (rc={rc})")
+        raise ValueError(f"the oracle rejected dims {dims.tolist()} (rc={rc})")
     return y
 
 
@@ -200,3 +233,26 @@ def unpack(dims, blob):
     if rc != 0:
         raise ValueError("or_unpack failed")
     return W, b
+
+
+def fp8_layout(dims):
+    """(region size, [image offsets, None for layer 0]) of the E4M3 images."""
+    dims = _dims_arr(dims)
+    L = len(dims) - 1
+    img = np.zeros(MAX_LAYERS, dtype=np.int64)
+    size = lib().or_fp8_layout(_ptr(dims), L, _ptr(img))
+    if size < 0:
+        raise ValueError(f"no E4M3 images for dims {dims.tolist()}")
+    return int(size), [None] + [int(v) for v in img[1:L]]
+
+
+def pack_fp8(dims, W) -> np.ndarray:
+    dims = _dims_arr(dims)
+    L = len(dims) - 1
+    size, _ = fp8_layout(dims)
+    W = [np.ascontiguousarray(w, dtype=np.uint16) for w in W]
+    region = np.zeros(size, dtype=np.uint8)
+    rc = lib().or_pack_fp8(_ptr(dims), L, _ptr_array(W), _ptr(region))
+    if rc != 0:
+        raise ValueError("or_pack_fp8 failed")
+    return region
