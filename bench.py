@@ -31,7 +31,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 CLOCK_FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-VARIANTS = {"fused": 0, "rowmajor": 1, "scalar": 2, "paired": 3}
+VARIANTS = {"fused": 0, "rowmajor": 1, "scalar": 2, "paired": 3, "fp8": 4}
+# Dense tensor rate of 8-bit E4M3 operands relative to FP16 (nominal figures:
+# 4.5 against 2.25 PFLOP/s per GPU), applied to the FP16 peak measured here.
+FP8_OVER_FP16 = 2.0
 
 
 def parse_args(argv=None):
@@ -206,25 +209,46 @@ def _oracle_sample(w, n_evals: int):
     return W, b, np.ascontiguousarray(x)
 
 
-def oracle_rate(w, n_evals: int, threads: int = 1):
+def oracle_forward(variant: str):
+    """The oracle's pass for a kernel variant: the E4M3 pass for the
+    narrow-precision variant, the FP16 pass for every other."""
+    import oracle
+    oracle.build()
+    return oracle.forward_fp8 if variant == "fp8" else oracle.forward
+
+
+def oracle_rate(w, n_evals: int, threads: int = 1, variant: str = "fused"):
     """Time the oracle, as it stands, on the first n_evals rows of a dispatch.
     With threads > 1 the rows are cut into contiguous ranges, each range one
     call of the (single-threaded) oracle, run on a thread pool: ctypes
     releases the GIL during the call, so the ranges run on that many cores."""
-    import oracle
-    oracle.build()
+    fwd = oracle_forward(variant)
     W, b, x = _oracle_sample(w, n_evals)
     t0 = time.perf_counter()
     if threads <= 1:
-        oracle.forward(w.dims, W, b, x)
+        fwd(w.dims, W, b, x)
     else:
         from concurrent.futures import ThreadPoolExecutor
         step = max(1, math.ceil(n_evals / (4 * threads)))
         with ThreadPoolExecutor(threads) as ex:
-            list(ex.map(lambda r0: oracle.forward(w.dims, W, b, x[r0:r0 + step]),
+            list(ex.map(lambda r0: fwd(w.dims, W, b, x[r0:r0 + step]),
                         range(0, n_evals, step)))
     dt = time.perf_counter() - t0
     return n_evals / dt / 1e6, dt
+
+
+def variant_dtype(variant: str) -> str:
+    return "e4m3 (layers 2..L) / f16 (layer 1)" if variant == "fp8" else "f16"
+
+
+def fp8_peak_split(w, fp16_tflops):
+    """The narrow-precision variant's tensor roofline: layer 1 at the FP16
+    peak, layers 2..L at FP8_OVER_FP16 times it. Returns the effective peak
+    (the network's FLOPs over the shortest time those two rates allow)."""
+    f1 = 2.0 * w.dims[0] * w.dims[1]
+    f8 = w.flops_per_eval - f1
+    t = f1 / fp16_tflops + f8 / (FP8_OVER_FP16 * fp16_tflops)
+    return w.flops_per_eval / t
 
 
 def host_cores() -> int:
@@ -239,11 +263,10 @@ def run_reference(args, w, rank):
     the workload per step, sized so the whole run takes about two minutes."""
     if rank != 0:
         return 0
-    import oracle
-    oracle.build()
+    fwd = oracle_forward(args.variant)
     K, W = args.steps if args.steps is not None else default_steps(w), args.warmup
     cores = host_cores()
-    _, dt = oracle_rate(w, 256)
+    _, dt = oracle_rate(w, 256, variant=args.variant)
     per_eval = dt / 256 / cores
     per_step = int(max(16 * cores, min(65536 * cores, 120.0 / (per_eval * max(1, K + W)))))
     Wt, bt, x = _oracle_sample(w, per_step)
@@ -252,7 +275,7 @@ def run_reference(args, w, rank):
     starts = range(0, per_step, span)
     with ThreadPoolExecutor(cores) as ex:
         def step():
-            list(ex.map(lambda r0: oracle.forward(w.dims, Wt, bt, x[r0:r0 + span]), starts))
+            list(ex.map(lambda r0: fwd(w.dims, Wt, bt, x[r0:r0 + span]), starts))
         for _ in range(W):
             step()
         t_total = 0.0
@@ -267,9 +290,10 @@ def run_reference(args, w, rank):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": K, "warmup": W, "ms_per_step": t_total / K * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-        "data": "synthetic",
-        "config": workload_config(w),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": variant_dtype(args.variant), "data": "synthetic",
+        "config": (dict(workload_config(w), variant=args.variant) if args.variant != "fused"
+                   else workload_config(w)),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -492,12 +516,18 @@ def main(argv=None):
     del lin, lout
 
     peaks, peaks_src = load_peaks()
-    bound, _, _ = roofline_bound(w, peaks, fp16_tflops)
+    tensor_peak = fp16_tflops
+    if args.variant == "fp8" and fp16_tflops:
+        tensor_peak = fp8_peak_split(w, fp16_tflops)
+    bound, _, _ = roofline_bound(w, peaks, tensor_peak)
     if bound == "tensor":
         achieved = w.flops_per_eval * n / (avg_kernel_ms * 1e-3) / 1e12
         if fp16_tflops:
-            peak, src = fp16_tflops, ("measured in this run: dense FP16 burst (torch.matmul FP16 "
+            peak, src = tensor_peak, ("measured in this run: dense FP16 burst (torch.matmul FP16 "
                                       "8192^3, best of 10, CUDA events)")
+            if args.variant == "fp8":
+                src += (f"; layers 2..L at {FP8_OVER_FP16:g}x that (the nominal FP8/FP16 ratio), "
+                        "layer 1 at the FP16 figure")
         else:
             peak, src = peaks["bf16_tflops"], f"{peaks_src}: dense bf16 burst"
         unit = "TFLOP/s"
@@ -515,7 +545,7 @@ def main(argv=None):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": Wu, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "vs_baseline": None, "dtype": variant_dtype(args.variant), "data": "synthetic",
         "config": dict(workload_config(w), variant=args.variant, l2=l2_note,
                        parallelism=f"replicas x{world}, no collective on the data path"),
         "roofline": roofline,
@@ -537,9 +567,9 @@ def main(argv=None):
         cores = host_cores()
         scale = 57344 / w.flops_per_eval  # about the same CPU time per workload
         all_n = min(w.n_evals, max(65536, int(1048576 * scale * cores / 16)))
-        v, dt = oracle_rate(w, all_n, threads=cores)
+        v, dt = oracle_rate(w, all_n, threads=cores, variant=args.variant)
         one_n = min(w.n_evals, max(16384, int(131072 * scale)))
-        v1, dt1 = oracle_rate(w, one_n)
+        v1, dt1 = oracle_rate(w, one_n, variant=args.variant)
         line["cpu_baseline"] = {
             "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"first {all_n:,} of the {w.n_evals:,} evaluations of one dispatch, "

@@ -69,9 +69,11 @@ typedef enum nm_status {
     NM_ERR_TIMEOUT = 6       /* a bounded wait inside a kernel gave up (see nm_mlp_device_status) */
 } nm_status;
 
-/* Kernel variants. NM_VARIANT_FUSED is the product path; the other two are
- * the page's two performance cliffs, kept as measured ablations. All three
- * produce bit-identical outputs. */
+/* Kernel variants. NM_VARIANT_FUSED is the product path; the row-major and
+ * scalar-activation variants are the page's two performance cliffs, kept as
+ * measured ablations; the paired-tiles variant is a measured alternative
+ * schedule. Those four produce bit-identical outputs. The narrow-precision
+ * variant computes differently (see its entry). */
 typedef enum nm_variant {
     /* Packed weights staged once per CTA into shared memory; packed half2
      * activation ("Row-major versus InferencingOptimal weights", optimal
@@ -92,7 +94,20 @@ typedef enum nm_variant {
      * 2 + 2 + 1). A larger M per issue than the default one tile per
      * issuing warp; measured slower on the benchmark networks, kept as a
      * measured alternative. Same arithmetic, bit-identical outputs. */
-    NM_VARIANT_PAIRED_TILES = 3
+    NM_VARIANT_PAIRED_TILES = 3,
+    /* Narrow-precision weights ("Optimization Techniques: Squeezing the
+     * Silicon", introduction: the FP16/quantization pillar; ninfer pull
+     * request #160: narrow weight codes streamed through a TMA ring). Layers
+     * 2..L multiply OCP E4M3 weights with E4M3 activations on the tensor
+     * cores (FP32 accumulation): the weights are rounded once at pack time,
+     * each hidden layer's FP16 activation is rounded to E4M3 (nearest even,
+     * saturating at +-448) as it is stored for the next layer. Layer 1, the
+     * biases and every layer's FP16 result and activation are as in the other
+     * variants. The weights always stream through the shared ring.
+     * Available when L >= 2 and every hidden width (dims[1] .. dims[L-1]) is
+     * a multiple of 32; otherwise nm_mlp_set_variant and nm_mlp_plan return
+     * NM_ERR_UNSUPPORTED. */
+    NM_VARIANT_FP8_WEIGHTS = 4
 } nm_variant;
 
 /* Version of this ABI (bumped on any incompatible change). */
@@ -121,10 +136,22 @@ nm_status nm_mlp_packed_size(const nm_mlp *h, size_t *bytes);
  * W: host array of L device pointers; W[l] is FP16 [dims[l+1]][dims[l]]
  *    row-major (row o holds the weights of output o).
  * b: host array of L device pointers; b[l] is FP16 [dims[l+1]].
- * The packed bits are a permutation of the input bits (no arithmetic).
+ * The packed bits are a permutation of the input bits (no arithmetic). For
+ * a network that has E4M3 images (nm_mlp_packed_fp8) the call also writes
+ * those, rounding every weight of W_2 .. W_L to E4M3.
  * Errors: NM_ERR_INVALID_ARG (NULL or misaligned pointer), NM_ERR_CUDA. */
 nm_status nm_mlp_pack_weights(nm_mlp *h, const void *const *W, const void *const *b,
                               nm_stream stream);
+
+/* The E4M3 weight images of NM_VARIANT_FP8_WEIGHTS, which nm_mlp_pack_weights
+ * writes beside the packed blob (same allocation, owned by the handle):
+ * device address and size in bytes (read-only; for byte-for-byte checks).
+ * Layout: the images of W_2 .. W_L in order, each starting at a multiple of
+ * 1024 bytes; an image's k range is cut into 128-, then 64-, then 32-column
+ * segments (1024-aligned, N rows of w bytes, 128/64/32-byte swizzle).
+ * Errors: NM_ERR_INVALID_ARG, NM_ERR_UNSUPPORTED (the network has no such
+ * images: L < 2 or a hidden width not a multiple of 32). */
+nm_status nm_mlp_packed_fp8(const nm_mlp *h, const void **region, size_t *bytes);
 
 /* Inverse of nm_mlp_pack_weights, into caller buffers of the same shapes.
  * Errors: NM_ERR_INVALID_ARG, NM_ERR_NOT_PACKED, NM_ERR_CUDA. */
@@ -181,7 +208,8 @@ nm_status nm_mlp_infer_host(nm_mlp *h, const void *host_in, int64_t n, void *hos
 nm_status nm_mlp_set_host_chunk(nm_mlp *h, int64_t rows);
 
 /* Select the kernel variant used by later nm_mlp_infer calls.
- * Errors: NM_ERR_INVALID_ARG for an unknown variant. */
+ * Errors: NM_ERR_INVALID_ARG for an unknown variant, NM_ERR_UNSUPPORTED for
+ * NM_VARIANT_FP8_WEIGHTS on a network without E4M3 images. */
 nm_status nm_mlp_set_variant(nm_mlp *h, nm_variant v);
 
 /* Synchronise `stream`, then read and clear the handle's device status word.

@@ -9,6 +9,7 @@
 // copied unchanged behind the weight images. Unpack is the same map run
 // backwards.
 #include <cuda.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -64,6 +65,76 @@ cudaError_t launch_pack(const PackParams& p, bool unpack, int num_sms, cudaStrea
   if (grid > 4 * num_sms) grid = 4 * num_sms;
   if (grid < 1) grid = 1;
   pack_kernel<<<grid, 256, 0, stream>>>(p, unpack ? 1 : 0);
+  return cudaGetLastError();
+}
+
+// E4M3 images: thread g rounds the 16 FP16 weights W_l[n][col .. col + 15]
+// (two 16-byte loads of one row) to E4M3 and stores them as one 16-byte
+// chunk. In the FP16-unit view of the image (K/2 columns of 2 bytes), the
+// chunk is the 8-column chunk at column col / 2.
+__global__ void __launch_bounds__(256) pack_fp8_kernel(const __grid_constant__ PackParams p,
+                                                       const __grid_constant__ Fp8Offsets o,
+                                                       uint8_t* region) {
+  const uint32_t total = o.chunk_start[p.L];
+  for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < total; g += gridDim.x * blockDim.x) {
+    int l = 1;
+    while (g >= o.chunk_start[l + 1]) ++l;
+    const uint32_t idx = g - o.chunk_start[l];
+    const int K = p.dims[l], N = p.dims[l + 1], kc = K >> 4;
+    const int n = static_cast<int>(idx / static_cast<uint32_t>(kc));
+    const int col = static_cast<int>(idx - static_cast<uint32_t>(n * kc)) << 4;
+    uint32_t off;
+    int w, k0;
+    locate(static_cast<uint32_t>(N), K >> 1, col >> 1, off, w, k0);
+    const uint32_t dst = o.off[l] + off + swz(static_cast<uint32_t>(n * 2 * w + (col - 2 * k0)), w);
+    const uint4* src = reinterpret_cast<const uint4*>(p.rm_w[l] + static_cast<size_t>(n) * K + col);
+    const uint4 a = __ldg(src), b = __ldg(src + 1);
+    const uint32_t hw[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __half2_raw h0, h1;
+      h0.x = static_cast<unsigned short>(hw[2 * j] & 0xFFFFu);
+      h0.y = static_cast<unsigned short>(hw[2 * j] >> 16);
+      h1.x = static_cast<unsigned short>(hw[2 * j + 1] & 0xFFFFu);
+      h1.y = static_cast<unsigned short>(hw[2 * j + 1] >> 16);
+      const uint32_t lo = __nv_cvt_halfraw2_to_fp8x2(h0, __NV_SATFINITE, __NV_E4M3);
+      const uint32_t hi = __nv_cvt_halfraw2_to_fp8x2(h1, __NV_SATFINITE, __NV_E4M3);
+      q[j] = lo | (hi << 16);
+    }
+    *reinterpret_cast<uint4*>(region + dst) = make_uint4(q[0], q[1], q[2], q[3]);
+  }
+}
+
+uint32_t fp8_layout(const int32_t* dims, int L, uint32_t* off) {
+  if (L < 2) return 0;
+  for (int l = 1; l < L; ++l)
+    if (dims[l] % 32 != 0) return 0;
+  uint32_t o = 0;
+  off[0] = 0;
+  for (int l = 1; l < L; ++l) {
+    o = align1024(o);
+    off[l] = o;
+    o += image_bytes(static_cast<uint32_t>(dims[l + 1]), dims[l] >> 1);
+  }
+  return o;
+}
+
+cudaError_t launch_pack_fp8(const PackParams& p, const uint32_t* fp8_off, uint8_t* region,
+                            int num_sms, cudaStream_t stream) {
+  Fp8Offsets o;
+  std::memset(&o, 0, sizeof(o));
+  uint32_t c = 0;
+  for (int l = 1; l < p.L; ++l) {
+    o.off[l] = fp8_off[l];
+    o.chunk_start[l] = c;
+    c += static_cast<uint32_t>(p.dims[l] * p.dims[l + 1] / 16);
+  }
+  o.chunk_start[p.L] = c;
+  int grid = static_cast<int>((c + 255u) / 256u);
+  if (grid > 4 * num_sms) grid = 4 * num_sms;
+  if (grid < 1) grid = 1;
+  pack_fp8_kernel<<<grid, 256, 0, stream>>>(p, o, region);
   return cudaGetLastError();
 }
 
@@ -211,6 +282,13 @@ struct nm_mlp {
   uint16_t* mirror = nullptr;    // row-major weights + biases for the row-major ablation
   uint32_t rm_b_off[nm::kMaxLayers] = {};
   size_t mirror_elems = 0;
+  // E4M3 images of the narrow-precision variant: in the blob's allocation
+  // from byte fp8_base on (fp8_size = 0: the network has none), with their
+  // own schedule (the FP16-unit view: K/2 columns, the images' offsets).
+  size_t fp8_base = 0;
+  size_t fp8_size = 0;
+  uint32_t fp8_off[nm::kMaxLayers] = {};
+  uint8_t* sched8 = nullptr;
   bool packed = false;
   bool mirror_valid = false;
   // A packing kernel (weights or the row-major mirror) was the last of this
@@ -310,6 +388,7 @@ nm_status launch_infer(nm_mlp* h, const void* in, int64_t n, void* out, cudaStre
   nm_status st = cached_io_maps(h, in, out, n);
   if (st != NM_OK) return st;
   FusedParams& p = h->params;
+  p.sched = h->variant == nm::kVarFp8 ? h->sched8 : h->sched;
   p.n = n;
   p.num_tiles = static_cast<int32_t>((n + nm::kTileM - 1) / nm::kTileM);
   p.wait_ns = h->wait_ns;
@@ -373,7 +452,7 @@ nm_status ensure_host_pipeline(nm_mlp* h) {
 
 extern "C" {
 
-int32_t nm_abi_version(void) { return 2; }
+int32_t nm_abi_version(void) { return 3; }
 
 const char* nm_status_str(nm_status s) {
   switch (s) {
@@ -392,7 +471,8 @@ nm_status nm_mlp_plan(const int32_t* dims, int32_t n_dims, nm_variant variant,
                       uint32_t smem_optin, nm_plan* plan) {
   if (!plan) return NM_ERR_INVALID_ARG;
   if (variant != NM_VARIANT_FUSED && variant != NM_VARIANT_ROWMAJOR_WEIGHTS &&
-      variant != NM_VARIANT_SCALAR_ACTIVATION && variant != NM_VARIANT_PAIRED_TILES)
+      variant != NM_VARIANT_SCALAR_ACTIVATION && variant != NM_VARIANT_PAIRED_TILES &&
+      variant != NM_VARIANT_FP8_WEIGHTS)
     return NM_ERR_INVALID_ARG;
   const nm_status dst = nm::check_dims(dims, n_dims);
   if (dst != NM_OK) return dst;
@@ -456,28 +536,42 @@ nm_status nm_mlp_create(const int32_t* dims, int32_t n_dims, nm_mlp** out) {
   }
   p.sched_bytes = nm::build_schedule(h->dims, L, h->w_off, h->rm_off, *sc, &p.bslab_bytes);
   nm::set_bias_params(*sc, dims, L, p);
+  h->fp8_size = nm::fp8_layout(h->dims, L, h->fp8_off);
+  h->fp8_base = h->fp8_size ? nm::align1024(static_cast<uint32_t>(h->blob_size)) : h->blob_size;
+  const size_t alloc = h->fp8_base + h->fp8_size;
 
-  if (cudaMalloc(&h->blob, h->blob_size) != cudaSuccess) {
+  if (cudaMalloc(&h->blob, alloc) != cudaSuccess) {
     delete sc;
     delete h;
     return NM_ERR_OOM;
   }
   if (cudaMalloc(&h->status, sizeof(uint32_t)) != cudaSuccess ||
-      cudaMalloc(&h->sched, sizeof(nm::Schedule)) != cudaSuccess) {
+      cudaMalloc(&h->sched, sizeof(nm::Schedule)) != cudaSuccess ||
+      (h->fp8_size && cudaMalloc(&h->sched8, sizeof(nm::Schedule)) != cudaSuccess)) {
     cudaFree(h->blob);
     if (h->status) cudaFree(h->status);
+    if (h->sched) cudaFree(h->sched);
     delete sc;
     delete h;
     return NM_ERR_OOM;
   }
-  const bool ok = cudaMemset(h->blob, 0, h->blob_size) == cudaSuccess &&
-                  cudaMemset(h->status, 0, sizeof(uint32_t)) == cudaSuccess &&
-                  cudaMemcpy(h->sched, sc, sizeof(nm::Schedule), cudaMemcpyHostToDevice) == cudaSuccess;
+  bool ok = cudaMemset(h->blob, 0, alloc) == cudaSuccess &&
+            cudaMemset(h->status, 0, sizeof(uint32_t)) == cudaSuccess &&
+            cudaMemcpy(h->sched, sc, sizeof(nm::Schedule), cudaMemcpyHostToDevice) == cudaSuccess;
+  if (ok && h->fp8_size) {
+    // Layers 2..L in the FP16-unit view of their E4M3 images.
+    for (int l = 1; l < L; ++l) {
+      sc->layer[l].K = h->dims[l] >> 1;
+      sc->layer[l].w_off = static_cast<uint32_t>(h->fp8_base) + h->fp8_off[l];
+    }
+    ok = cudaMemcpy(h->sched8, sc, sizeof(nm::Schedule), cudaMemcpyHostToDevice) == cudaSuccess;
+  }
   delete sc;
   if (!ok) {
     cudaFree(h->blob);
     cudaFree(h->status);
     cudaFree(h->sched);
+    if (h->sched8) cudaFree(h->sched8);
     delete h;
     return NM_ERR_CUDA;
   }
@@ -500,6 +594,14 @@ nm_status nm_mlp_packed_blob(const nm_mlp* h, const void** blob) {
   return NM_OK;
 }
 
+nm_status nm_mlp_packed_fp8(const nm_mlp* h, const void** region, size_t* bytes) {
+  if (!h || !region || !bytes) return NM_ERR_INVALID_ARG;
+  if (!h->fp8_size) return NM_ERR_UNSUPPORTED;
+  *region = h->blob + h->fp8_base;
+  *bytes = h->fp8_size;
+  return NM_OK;
+}
+
 nm_status nm_mlp_pack_weights(nm_mlp* h, const void* const* W, const void* const* b,
                               nm_stream stream) {
   if (!h || !W || !b) return NM_ERR_INVALID_ARG;
@@ -510,6 +612,10 @@ nm_status nm_mlp_pack_weights(nm_mlp* h, const void* const* W, const void* const
     pp.rm_b[l] = const_cast<uint16_t*>(static_cast<const uint16_t*>(b[l]));
   }
   if (nm::launch_pack(pp, false, h->num_sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return NM_ERR_CUDA;
+  if (h->fp8_size &&
+      nm::launch_pack_fp8(pp, h->fp8_off, h->blob + h->fp8_base, h->num_sms,
+                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return NM_ERR_CUDA;
   h->packed = true;
   h->mirror_valid = false;
@@ -604,8 +710,9 @@ nm_status nm_mlp_set_host_chunk(nm_mlp* h, int64_t rows) {
 nm_status nm_mlp_set_variant(nm_mlp* h, nm_variant v) {
   if (!h) return NM_ERR_INVALID_ARG;
   if (v != NM_VARIANT_FUSED && v != NM_VARIANT_ROWMAJOR_WEIGHTS && v != NM_VARIANT_SCALAR_ACTIVATION &&
-      v != NM_VARIANT_PAIRED_TILES)
+      v != NM_VARIANT_PAIRED_TILES && v != NM_VARIANT_FP8_WEIGHTS)
     return NM_ERR_INVALID_ARG;
+  if (v == NM_VARIANT_FP8_WEIGHTS && !h->fp8_size) return NM_ERR_UNSUPPORTED;
   h->variant = static_cast<int>(v);
   return NM_OK;
 }
@@ -646,6 +753,7 @@ void nm_mlp_destroy(nm_mlp* h) {
   cudaFree(h->blob);
   cudaFree(h->status);
   cudaFree(h->sched);
+  if (h->sched8) cudaFree(h->sched8);
   if (h->mirror) cudaFree(h->mirror);
   delete h;
 }

@@ -47,6 +47,7 @@
 // (with a fixed limit) for its own copies and MMAs in flight, and the CTA
 // frees its tensor memory and exits.
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <atomic>
 #include <cstring>
@@ -86,8 +87,12 @@ __host__ __device__ constexpr bool is_scalar_act(int V) {
 }
 
 __host__ __device__ constexpr bool is_stream(int V) {
-  return V == kVarFusedStream || V == kVarScalarStream;
+  return V == kVarFusedStream || V == kVarScalarStream || V == kVarFp8Stream;
 }
+
+// Layers 2..L take E4M3 operands (A: the previous layer's activations,
+// rounded as the epilogue stores them; B: the weights' E4M3 images).
+__host__ __device__ constexpr bool is_fp8(int V) { return V == kVarFp8Stream; }
 
 // LayerInfo as loaded from shared memory (two 16-byte loads).
 struct LayerRegs {
@@ -204,6 +209,35 @@ __device__ __forceinline__ void convert_pairs(const uint32_t* acc, __half2 slope
       out[j] = *reinterpret_cast<uint32_t*>(&h);
     }
   }
+}
+
+// The narrow-precision variant's hidden-layer epilogue: FP32 accumulator
+// pairs -> FP16 pairs (nearest even) -> activation (as convert_pairs) ->
+// E4M3 pairs (nearest even, saturating at 448), packed four to a 32-bit
+// TMEM column with the lowest K in the lowest byte. NP pairs, NP / 2 words.
+template <int NP>
+__device__ __forceinline__ void convert_pairs_e4m3(const uint32_t* acc, __half2 slope2,
+                                                   uint32_t* out) {
+#pragma unroll
+  for (int j = 0; j < NP / 2; ++j) {
+    __half2 h0 = __floats2half2_rn(__uint_as_float(acc[4 * j]), __uint_as_float(acc[4 * j + 1]));
+    __half2 h1 = __floats2half2_rn(__uint_as_float(acc[4 * j + 2]), __uint_as_float(acc[4 * j + 3]));
+    h0 = __hmax2(h0, __hmul2(h0, slope2));
+    h1 = __hmax2(h1, __hmul2(h1, slope2));
+    const uint32_t lo = __nv_cvt_halfraw2_to_fp8x2(static_cast<__half2_raw>(h0), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_halfraw2_to_fp8x2(static_cast<__half2_raw>(h1), __NV_SATFINITE, __NV_E4M3);
+    out[j] = lo | (hi << 16);
+  }
+}
+
+// A-in-TMEM MMA of one K slab: FP16 operands, or E4M3 ones (F8).
+template <bool F8>
+__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  if constexpr (F8)
+    umma_f8_ts(d, a, b, idesc, accumulate);
+  else
+    umma_f16_ts(d, a, b, idesc, accumulate);
 }
 
 // A layer's k-slab MMAs are issued in groups of up to four, each group a
@@ -511,10 +545,10 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
         tc_fence_after_sync();
         const uint64_t bd = desc64 + ((c.sbase + p.sm_wring + ws * p.wstage_bytes) >> 4);
         const uint32_t at = slot_tmem + p.a_col + 32u * static_cast<uint32_t>(j);
-        umma_f16_ts(slot_tmem, at, bd, li.idesc, j > 0 ? 1u : 0u);
-        umma_f16_ts(slot_tmem, at + 8u, bd + 2u, li.idesc, 1u);
-        umma_f16_ts(slot_tmem, at + 16u, bd + 4u, li.idesc, 1u);
-        umma_f16_ts(slot_tmem, at + 24u, bd + 6u, li.idesc, 1u);
+        umma_ts<is_fp8(V)>(slot_tmem, at, bd, li.idesc, j > 0 ? 1u : 0u);
+        umma_ts<is_fp8(V)>(slot_tmem, at + 8u, bd + 2u, li.idesc, 1u);
+        umma_ts<is_fp8(V)>(slot_tmem, at + 16u, bd + 4u, li.idesc, 1u);
+        umma_ts<is_fp8(V)>(slot_tmem, at + 24u, bd + 6u, li.idesc, 1u);
         umma_commit(c.bar(kBarWEmpty + ws));
         next_stage();
       }
@@ -544,11 +578,11 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
         }
       } else {
         const uint32_t at = slot_tmem + p.a_col + (static_cast<uint32_t>(k0) >> 1);
-        umma_f16_ts(slot_tmem, at, bd, li.idesc, acc0);
-        if (w >= 32) umma_f16_ts(slot_tmem, at + 8u, bd + 2u, li.idesc, 1u);
+        umma_ts<is_fp8(V)>(slot_tmem, at, bd, li.idesc, acc0);
+        if (w >= 32) umma_ts<is_fp8(V)>(slot_tmem, at + 8u, bd + 2u, li.idesc, 1u);
         if (w == 64) {
-          umma_f16_ts(slot_tmem, at + 16u, bd + 4u, li.idesc, 1u);
-          umma_f16_ts(slot_tmem, at + 24u, bd + 6u, li.idesc, 1u);
+          umma_ts<is_fp8(V)>(slot_tmem, at + 16u, bd + 4u, li.idesc, 1u);
+          umma_ts<is_fp8(V)>(slot_tmem, at + 24u, bd + 6u, li.idesc, 1u);
         }
       }
       umma_commit(c.bar(kBarWEmpty + ws));
@@ -624,13 +658,21 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
       if (ok) {
         tc_fence_after_sync();
         for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
-          uint32_t acc[32], h[16];
+          uint32_t acc[32];
           tmem_ld_x32(tbase + static_cast<uint32_t>(c0), acc);
           tmem_wait_ld();
-          convert_pairs<V, 16, true>(acc, slope2, h);
-          tmem_st_x16(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
+          if constexpr (is_fp8(V)) {
+            uint32_t q[8];
+            convert_pairs_e4m3<16>(acc, slope2, q);
+            tmem_st_x8(a_tmem + static_cast<uint32_t>(c0 >> 2), q);
+          } else {
+            uint32_t h[16];
+            convert_pairs<V, 16, true>(acc, slope2, h);
+            tmem_st_x16(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
+          }
         }
-        if ((N & 31) && ((N >> 5) % G) == g) {
+        // (hidden widths of the narrow-precision variant are multiples of 32)
+        if (!is_fp8(V) && (N & 31) && ((N >> 5) % G) == g) {
           const int c0 = N - 16;
           uint32_t acc[16], h[8];
           tmem_ld_x16(tbase + static_cast<uint32_t>(c0), acc);
@@ -1337,11 +1379,19 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
   // buffers before one. If the weights do not fit (fused and
   // scalar-activation variants), stream them with at most 2 slots and the
   // deepest weight ring (4 down to 2 stages) that fits.
-  for (int mode = 0; mode < 2; ++mode) {
+  // The narrow-precision variant: streamed weights only, on networks that
+  // have E4M3 images; its A region holds four E4M3 values per column.
+  const bool fp8 = variant == kVarFp8;
+  if (fp8) {
+    if (L < 2) return 0;
+    for (int l = 1; l < L; ++l)
+      if (dims[l] % 32 != 0) return 0;
+  }
+  for (int mode = fp8 ? 1 : 0; mode < 2; ++mode) {
     const bool streamed = mode == 1;
     if (streamed && variant == kVarRowMajor) break;
     p.a_col = acc_cols;
-    p.slot_cols = acc_cols + (((hmax / 2u) + 31u) & ~31u);
+    p.slot_cols = acc_cols + (((hmax / (fp8 ? 4u : 2u)) + 31u) & ~31u);
     const uint32_t max_slots = streamed ? static_cast<uint32_t>(kStreamSlots) : static_cast<uint32_t>(kMaxSlots);
     for (uint32_t slots = max_slots; slots >= 1; --slots) {
       const uint32_t used = slots * p.slot_cols + 32u;
@@ -1462,6 +1512,7 @@ cudaError_t launch_fused(const FusedParams& p, int variant, int grid, uint32_t s
     if (variant == kVarFused || variant == kVarPaired)
       return launch_variant<kVarFusedStream>(p, grid, smem, stream, overlap);
     if (variant == kVarScalar) return launch_variant<kVarScalarStream>(p, grid, smem, stream, overlap);
+    if (variant == kVarFp8) return launch_variant<kVarFp8Stream>(p, grid, smem, stream, overlap);
     return cudaErrorInvalidValue;
   }
   switch (variant) {

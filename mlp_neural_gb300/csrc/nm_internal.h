@@ -29,9 +29,10 @@ constexpr int kOutBufs = 2;        // output staging buffers per slot (TMA-store
 constexpr int kMaxSlabs = kMaxLayers * (kMaxDim / 16);
 constexpr uint32_t kStatusTimeout = 1u;
 
-// Public variants 0..3 (nm_variant); 4 and 5 are the fused and the
+// Public variants 0..4 (nm_variant); 8 and 9 are the fused and the
 // scalar-activation kernels with streamed instead of resident weights, chosen
-// by the planner when the packed weights do not fit in shared memory. The
+// by the planner when the packed weights do not fit in shared memory; 10 is
+// the narrow-precision variant, which always streams its weights. The
 // paired-tiles variant runs the fused kernel with a plan that issues the tile
 // regions two at a time.
 enum Variant : int {
@@ -39,8 +40,10 @@ enum Variant : int {
   kVarRowMajor = 1,
   kVarScalar = 2,
   kVarPaired = 3,
-  kVarFusedStream = 4,
-  kVarScalarStream = 5
+  kVarFp8 = 4,
+  kVarFusedStream = 8,
+  kVarScalarStream = 9,
+  kVarFp8Stream = 10
 };
 constexpr int kMaxWStages = 4;     // streamed-weight ring depth (upper bound)
 
@@ -157,6 +160,20 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
 cudaError_t launch_fused(const FusedParams& p, int variant, int grid, uint32_t smem,
                          cudaStream_t stream, bool overlap);
 
+// Per-layer offsets of the E4M3 images and the first 16-byte chunk of each
+// layer (layers 1..L-1) for the E4M3 packing kernel.
+struct Fp8Offsets {
+  uint32_t off[kMaxLayers];
+  uint32_t chunk_start[kMaxLayers + 1];
+};
+
+// E4M3 weight images of the narrow-precision variant (layers 1..L-1, 0-based):
+// byte layout of a K-wide FP16 image with K/2 columns, 1024-aligned image
+// starts. Requires L >= 2 and hidden widths that are multiples of 32.
+// Fills off[l] (l >= 1, relative to the region's start) and returns the
+// region's size, or 0 when the network has no such images.
+uint32_t fp8_layout(const int32_t* dims, int L, uint32_t* off);
+
 struct PackParams {
   int32_t L;
   int32_t dims[kMaxLayers + 1];
@@ -170,6 +187,13 @@ struct PackParams {
 };
 
 cudaError_t launch_pack(const PackParams& p, bool unpack, int num_sms, cudaStream_t stream);
+
+// Writes the E4M3 images (fp8_layout) of W_1..W_{L-1} from the row-major
+// FP16 weights p.rm_w into `region`: each thread rounds 16 weights of one row
+// (round to nearest even, saturating at 448) and stores them as one swizzled
+// 16-byte chunk.
+cudaError_t launch_pack_fp8(const PackParams& p, const uint32_t* fp8_off, uint8_t* region,
+                            int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------- host helpers
 // Shared by every entry point that launches the kernels (nm_api.cu for the

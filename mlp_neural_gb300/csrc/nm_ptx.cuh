@@ -240,6 +240,20 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Same with 8-bit E4M3 operands (kind::f8f6f4; the instruction descriptor's
+// A and B format fields are 0 = E4M3): one MMA covers K = 32, the A slab
+// spans the same 8 TMEM columns (four consecutive K elements per column,
+// lowest K in the lowest byte) and the B slab the same 32 bytes per row.
+__device__ __forceinline__ void umma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued before
 // has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {

@@ -24,6 +24,7 @@ NM_VARIANT_FUSED = 0
 NM_VARIANT_ROWMAJOR_WEIGHTS = 1
 NM_VARIANT_SCALAR_ACTIVATION = 2
 NM_VARIANT_PAIRED_TILES = 3
+NM_VARIANT_FP8_WEIGHTS = 4
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnmmlp.so")
 
@@ -37,6 +38,7 @@ SIGNATURES = {
     "nm_mlp_pack_weights": (ctypes.c_int, [_P, _P, _P, _P]),
     "nm_mlp_unpack_weights": (ctypes.c_int, [_P, _P, _P, _P]),
     "nm_mlp_packed_blob": (ctypes.c_int, [_P, ctypes.POINTER(_P)]),
+    "nm_mlp_packed_fp8": (ctypes.c_int, [_P, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]),
     "nm_mlp_infer": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P, _P]),
     "nm_mlp_infer_host": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P, _P]),
     "nm_mlp_set_host_chunk": (ctypes.c_int, [_P, ctypes.c_int64]),
@@ -175,6 +177,13 @@ class MLP:
         p = ctypes.c_void_p()
         _check(lib().nm_mlp_packed_blob(self._h, ctypes.byref(p)), "nm_mlp_packed_blob")
         return p.value
+
+    def packed_fp8(self):
+        """(device address, bytes) of the E4M3 weight images."""
+        p = _P()
+        n = ctypes.c_size_t()
+        _check(lib().nm_mlp_packed_fp8(self._h, ctypes.byref(p), ctypes.byref(n)), "nm_mlp_packed_fp8")
+        return int(p.value or 0), int(n.value)
 
     def pack_weights(self, W, b, stream=None):
         Wp = (ctypes.c_void_p * len(W))(*[_addr(w) for w in W])

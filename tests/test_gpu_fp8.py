@@ -1,0 +1,143 @@
+"""GPU parity of the narrow-precision variant (NM_VARIANT_FP8_WEIGHTS) against
+the oracle's E4M3 pass (or_mlp_forward_fp8), through the C ABI.
+
+Bars:
+ - the E4M3 weight images bit-exact against the oracle's packer;
+ - bit-exact outputs on networks whose FP32 sums are exact (E4M3 weights with
+   a narrow exponent range, 8-bit inputs), where the tensor core's summation
+   order cannot matter;
+ - on random networks, the GPU and the oracle compute the same quantized
+   network and differ only through the order of the FP32 sums. A different
+   order moves a sum by a few FP32 ulps, which now and then moves an FP16 or
+   an E4M3 rounding to the neighbouring value. An E4M3 step is 2^-3 of its
+   binade, and it reaches the outputs through the later layers, so the rare
+   rows it touches can differ by a tenth or more while every other row is
+   identical. (A float64-sum restatement of the same network, which differs
+   from the oracle the same way, changes 0.01-0.02 % of the rows of the
+   wide and heterogeneous networks, by at most 0.21.) The bar is therefore
+   per row: at most FP8_ROW_FRAC of the rows may differ from the oracle at
+   all, and no element by more than FP8_TOL_ABS + FP8_TOL_REL |cpu|.
+"""
+import numpy as np
+import pytest
+
+from mlp_neural_gb300 import synth
+from gpu_util import make_net, nm, read_device, to_dev, to_host
+from netgen import exact_fp8_net
+
+pytestmark = pytest.mark.gpu
+
+FP8_ROW_FRAC = 2e-3
+FP8_TOL_ABS = 0.5
+FP8_TOL_REL = 0.1
+
+FP8_DIMS = [synth.WORKLOADS["wide"].dims, synth.WORKLOADS["hetero"].dims,
+            (48, 96, 224, 32, 16),          # segments of 128/64/32 E4M3 columns
+            (64, 160, 16),                  # one E4M3 layer
+            (32, 64, 64, 64, 64, 64, 64, 64, 16),
+            (80,) + (96,) * 8 + (16,)]      # K tails in both precisions
+
+
+def _infer(m, x16, extra_rows=0):
+    import torch
+    n = x16.shape[0]
+    out = torch.zeros((n + extra_rows, m.dims[-1]), dtype=torch.float16, device="cuda")
+    m.set_variant(nm().NM_VARIANT_FP8_WEIGHTS)
+    m.infer(to_dev(x16), out[:n])
+    torch.cuda.synchronize()
+    assert m.device_status() == nm().NM_OK
+    y = to_host(out)
+    assert (y[n:] == 0).all(), "rows beyond n were written"
+    return y[:n]
+
+
+def fp8_compare(gpu16, cpu16, what=""):
+    """Row bar of the module docstring; returns (differing rows, max |gpu-cpu|)."""
+    g = gpu16.view(np.float16).astype(np.float64)
+    c = cpu16.view(np.float16).astype(np.float64)
+    assert g.shape == c.shape
+    assert np.isfinite(g).all(), what
+    err = np.abs(g - c)
+    rows = int((err.max(axis=1) > 0).sum()) if err.size else 0
+    assert rows <= max(1, FP8_ROW_FRAC * g.shape[0]), \
+        f"{what}: {rows} of {g.shape[0]} rows differ from the oracle"
+    bad = np.argwhere(err > FP8_TOL_ABS + FP8_TOL_REL * np.abs(c))
+    assert bad.size == 0, f"{what}: element {bad[0].tolist()} gpu={g[tuple(bad[0])]} cpu={c[tuple(bad[0])]}"
+    return rows, float(err.max()) if err.size else 0.0
+
+
+@pytest.mark.parametrize("dims", FP8_DIMS)
+def test_fp8_images_bit_exact(orc, dims):
+    W, b, _ = synth.small_net_inputs(dims, seed=31, n=1)
+    m = make_net(dims, W, b)
+    ptr, size = m.packed_fp8()
+    ref = orc.pack_fp8(dims, W)
+    assert size == ref.size
+    assert np.array_equal(read_device(ptr, size), ref)
+    # the FP16 blob is unchanged by the extra images
+    assert np.array_equal(read_device(m.packed_blob(), m.packed_size()), orc.pack(dims, W, b))
+
+
+@pytest.mark.parametrize("dims", FP8_DIMS[:4])
+def test_fp8_exact_networks_bit_exact(orc, dims):
+    W, b = exact_fp8_net(dims, seed=7 + sum(dims))
+    rng = np.random.default_rng(dims[1])
+    n = 152 * 128 * 2 + 77   # every CTA, several rounds, a ragged tail
+    x = (rng.integers(-255, 256, size=(n, dims[0])) * 2.0 ** -8).astype(np.float16).view(np.uint16)
+    m = make_net(dims, W, b)
+    y = _infer(m, x, extra_rows=200)
+    ref = orc.forward_fp8(dims, W, b, x)
+    assert np.array_equal(y, ref), f"{int((y != ref).any(axis=1).sum())} rows differ"
+    # and the variant really is narrower than the FP16 path
+    assert not np.array_equal(ref, orc.forward(dims, W, b, x))
+
+
+@pytest.mark.parametrize("dims", FP8_DIMS)
+@pytest.mark.parametrize("n", [1, 129, 4097])
+def test_fp8_matches_oracle(orc, dims, n):
+    W, b, x = synth.small_net_inputs(dims, seed=n + dims[1], n=n)
+    m = make_net(dims, W, b)
+    y = _infer(m, x, extra_rows=130)
+    rows, emax = fp8_compare(y, orc.forward_fp8(dims, W, b, x), f"dims={dims} n={n}")
+    print(f"dims={dims} n={n}: {rows} rows differ, max |gpu-cpu| = {emax:.3g}")
+
+
+@pytest.mark.parametrize("name", ["wide", "hetero"])
+def test_fp8_full_workload_one_row_per_tile(orc, name):
+    """The full workload through the FP8 variant in one dispatch; one row of
+    every 128-row tile (the row inside the tile rotates with the tile index)
+    against the oracle, plus the first and last tile whole."""
+    import torch
+    from concurrent.futures import ThreadPoolExecutor
+    w = synth.WORKLOADS[name]
+    W, b = synth.net_params(w.dims, w.seed)
+    x = synth.inputs(w)
+    m = make_net(w.dims, W, b)
+    m.set_variant(nm().NM_VARIANT_FP8_WEIGHTS)
+    xd = to_dev(x)
+    out = torch.empty((w.n_evals, w.dims[-1]), dtype=torch.float16, device="cuda")
+    m.infer(xd, out)
+    torch.cuda.synchronize()
+    assert m.device_status() == nm().NM_OK
+    y = to_host(out)
+    n = x.shape[0]
+    tiles = (n + 127) // 128
+    rows = np.minimum(np.arange(tiles) * 128 + (np.arange(tiles) * 37) % 128, n - 1)
+    rows = np.unique(np.concatenate([rows, np.arange(128), np.arange(n - 128, n)]))
+    parts = np.array_split(rows, 64)
+    with ThreadPoolExecutor() as ex:
+        refs = list(ex.map(lambda r: orc.forward_fp8(w.dims, W, b, x[r]), parts))
+    diff, emax = fp8_compare(y[rows], np.concatenate(refs), name)
+    print(f"{name} FP8: {rows.size:,} rows checked, {diff} differ, max |gpu-cpu| = {emax:.3g}")
+
+
+def test_fp8_variant_needs_e4m3_images():
+    lib = nm()
+    W, b, _ = synth.small_net_inputs((32, 48, 16), seed=1, n=1)
+    m = make_net((32, 48, 16), W, b)
+    with pytest.raises(lib.NmError) as e:
+        m.set_variant(lib.NM_VARIANT_FP8_WEIGHTS)
+    assert e.value.status == lib.NM_ERR_UNSUPPORTED
+    with pytest.raises(lib.NmError) as e:
+        m.packed_fp8()
+    assert e.value.status == lib.NM_ERR_UNSUPPORTED

@@ -24,6 +24,7 @@ import pytest
 import torch
 
 from mlp_neural_gb300 import synth
+from netgen import exact_fp8_net
 
 SLOPE = np.float16(0.01)
 
@@ -68,24 +69,6 @@ def test_e4m3_encode_saturates_and_keeps_nan(orc):
     assert orc.f16_to_e4m3_array(np.array([1.0625, 1.1875], np.float16).view(np.uint16)).tolist() == [0x38, 0x3A]
 
 
-def _exact_net(dims, seed):
-    """A network whose FP32 sums are exact: every weight of layers >= 2 is
-    E4M3 with exponent in [-4, -1]; layer-1 weights have 8 significant bits
-    (E4M3 cannot hold most of them); biases are multiples of 2^-8 below 1/4."""
-    rng = np.random.default_rng(seed)
-    W, b = [], []
-    for l in range(len(dims) - 1):
-        K, N = dims[l], dims[l + 1]
-        sgn = rng.choice([-1.0, 1.0], size=(N, K))
-        if l == 0:
-            v = sgn * rng.integers(128, 256, size=(N, K)) * 2.0 ** rng.integers(-12, -8, size=(N, K))
-        else:
-            v = sgn * (8 + rng.integers(0, 8, size=(N, K))) * 2.0 ** rng.integers(-7, -4, size=(N, K))
-        W.append(v.astype(np.float16).view(np.uint16))
-        b.append((rng.integers(-64, 64, size=N) * 2.0 ** -8).astype(np.float16).view(np.uint16))
-    return W, b
-
-
 def _brute_fp8(dims, W, b, x):
     cur = x.view(np.float16).astype(np.float64)
     L = len(dims) - 1
@@ -103,7 +86,7 @@ def _brute_fp8(dims, W, b, x):
 
 @pytest.mark.parametrize("dims", [(32, 64, 32, 16), (64, 128, 128, 16), (48, 96, 64, 160, 32)])
 def test_forward_fp8_against_brute_force(orc, dims):
-    W, b = _exact_net(dims, seed=sum(dims))
+    W, b = exact_fp8_net(dims, seed=sum(dims))
     rng = np.random.default_rng(7)
     x = (rng.integers(-255, 256, size=(300, dims[0])) * 2.0 ** -8).astype(np.float16).view(np.uint16)
     got = orc.forward_fp8(dims, W, b, x)

@@ -32,14 +32,29 @@ def _threads(slots, warps, streamed):
     return 32 * (slots * warps + 2) if streamed else 32 * (8 + slots * warps)
 
 
-def _tmem_needed(dims, slots):
-    # per slot: the FP32 accumulator of the widest layer and the FP16 pairs of
-    # the widest hidden layer (each rounded up to 32 columns), plus one
+def _tmem_needed(dims, slots, per_col=2):
+    # per slot: the FP32 accumulator of the widest layer and the next layer's
+    # A for the widest hidden layer (FP16 pairs, or E4M3 quads for the
+    # narrow-precision variant; each rounded up to 32 columns), plus one
     # 32-column block for the shared ones slab
     r32 = lambda c: (c + 31) // 32 * 32
     acc = r32(max(dims[1:]))
     hidden = max([16] + list(dims[1:-1]))
-    return slots * (acc + r32(hidden // 2)) + 32
+    return slots * (acc + r32(hidden // per_col)) + 32
+
+
+@pytest.mark.parametrize("name,slots,warps", [("wide", 2, 8), ("hetero", 1, 16), ("page", 2, 8)])
+def test_fp8_plans_stream_their_weights(nmlib, name, slots, warps):
+    p = nmlib.plan(synth.WORKLOADS[name].dims, nmlib.NM_VARIANT_FP8_WEIGHTS)
+    assert (p["tile_slots"], p["warps_per_slot"], p["streamed_weights"]) == (slots, warps, 1)
+    assert p["threads"] == _threads(slots, warps, 1)
+
+
+@pytest.mark.parametrize("dims", [(32, 16), (32, 48, 16), (64, 128, 80, 16)])
+def test_fp8_plan_needs_e4m3_images(nmlib, dims):
+    with pytest.raises(nmlib.NmError) as e:
+        nmlib.plan(dims, nmlib.NM_VARIANT_FP8_WEIGHTS)
+    assert e.value.status == nmlib.NM_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("name,fused_issuers,paired_issuers", [
@@ -54,13 +69,17 @@ def test_issuing_warps(nmlib, name, fused_issuers, paired_issuers):
     assert p["tile_slots"] == nmlib.plan(dims)["tile_slots"]
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
 def test_plan_invariants_over_random_networks(nmlib, variant):
     rng = np.random.default_rng(100 + variant)
     planned = 0
     for _ in range(400):
         L = int(rng.integers(1, 17))
         dims = [int(16 * rng.integers(1, 17)) for _ in range(L + 1)]
+        if variant == 4:  # hidden widths that have E4M3 images
+            L = max(L, 2)
+            dims = ([int(16 * rng.integers(1, 17))] + [int(32 * rng.integers(1, 9)) for _ in range(L - 1)]
+                    + [int(16 * rng.integers(1, 17))])
         try:
             p = nmlib.plan(dims, variant)
         except nmlib.NmError as e:
@@ -73,13 +92,15 @@ def test_plan_invariants_over_random_networks(nmlib, variant):
         assert p["smem_bytes"] <= nmlib.GB300_SMEM_OPTIN
         t = p["tmem_columns"]
         assert 32 <= t <= 512 and t & (t - 1) == 0
-        assert _tmem_needed(dims, slots) <= t
+        assert _tmem_needed(dims, slots, 4 if variant == 4 else 2) <= t
         assert p["input_stages"] in (1, 2) and p["output_buffers"] in (1, 2)
         if p["streamed_weights"]:
             assert variant != 1 and slots <= 2 and 2 <= p["weight_stages"] <= 4
+            if variant == 4:
+                assert all(d % 32 == 0 for d in dims[1:-1]) and L >= 2
             assert p["issuing_warps"] == slots
         else:
-            assert p["weight_stages"] == 0
+            assert variant != 4 and p["weight_stages"] == 0
             paired = variant == 3 and warps == 4
             assert p["issuing_warps"] == ((slots + 1) // 2 if paired else slots)
     assert planned > 200
