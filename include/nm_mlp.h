@@ -291,6 +291,9 @@ typedef struct nm_plan {
   uint32_t tmem_columns;    /* tensor memory columns allocated per CTA */
   int32_t issuing_warps;    /* warps that issue MMA chains (one per slot, or per pair of
                                slots with NM_VARIANT_PAIRED_TILES) */
+  int32_t a_tmem_k;         /* columns of the next layer's A kept in tensor memory; a
+                               streamed FP16 plan may keep the rest (whole 64-column
+                               segments) in shared memory to fit one more tile slot */
 } nm_plan;
 
 nm_status nm_mlp_plan(const int32_t *dims, int32_t n_dims, nm_variant variant,

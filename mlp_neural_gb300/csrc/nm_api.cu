@@ -499,6 +499,7 @@ nm_status nm_mlp_plan(const int32_t* dims, int32_t n_dims, nm_variant variant,
   plan->tmem_columns = p.tmem_cols;
   plan->issuing_warps = p.stream_w ? static_cast<int32_t>(p.n_slots)
                                    : static_cast<int32_t>(p.n_groups_issue);
+  plan->a_tmem_k = static_cast<int32_t>(p.a_tmem_k);
   return NM_OK;
 }
 

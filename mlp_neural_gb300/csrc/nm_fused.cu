@@ -474,6 +474,7 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
   const int32_t n_rounds = (c.n_local - s + S - 1) / S;  // tiles r*S + s < n_local
   const bool storer = (lane == 0) && (32 * g < n_out);
   const uint32_t b_stage = c.sbase + p.sm_b + static_cast<uint32_t>(s) * p.b_stage_bytes;
+  const uint32_t a_smem = c.sbase + p.sm_a + static_cast<uint32_t>(s) * p.a_smem_bytes;
 
   // Row-major ablation: this warp's share (rows wi, wi + nw, ...) of W_l
   // rebuilt in the slot's B stage, 16-byte loads, swizzled 16-byte stores.
@@ -544,11 +545,21 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
         if (!ok) break;
         tc_fence_after_sync();
         const uint64_t bd = desc64 + ((c.sbase + p.sm_wring + ws * p.wstage_bytes) >> 4);
-        const uint32_t at = slot_tmem + p.a_col + 32u * static_cast<uint32_t>(j);
-        umma_ts<is_fp8(V)>(slot_tmem, at, bd, li.idesc, j > 0 ? 1u : 0u);
-        umma_ts<is_fp8(V)>(slot_tmem, at + 8u, bd + 2u, li.idesc, 1u);
-        umma_ts<is_fp8(V)>(slot_tmem, at + 16u, bd + 4u, li.idesc, 1u);
-        umma_ts<is_fp8(V)>(slot_tmem, at + 24u, bd + 6u, li.idesc, 1u);
+        const uint32_t kj = 64u * static_cast<uint32_t>(j);
+        if (is_fp8(V) || kj < p.a_tmem_k) {
+          const uint32_t at = slot_tmem + p.a_col + (kj >> 1);
+          umma_ts<is_fp8(V)>(slot_tmem, at, bd, li.idesc, j > 0 ? 1u : 0u);
+          umma_ts<is_fp8(V)>(slot_tmem, at + 8u, bd + 2u, li.idesc, 1u);
+          umma_ts<is_fp8(V)>(slot_tmem, at + 16u, bd + 4u, li.idesc, 1u);
+          umma_ts<is_fp8(V)>(slot_tmem, at + 24u, bd + 6u, li.idesc, 1u);
+        } else {
+          // this segment of A is in the slot's shared-memory A buffer
+          const uint64_t ad = desc64 + ((a_smem + 128u * (kj - p.a_tmem_k) * 2u) >> 4);
+          umma_f16_ss(slot_tmem, ad, bd, li.idesc, j > 0 ? 1u : 0u);
+          umma_f16_ss(slot_tmem, ad + 2u, bd + 2u, li.idesc, 1u);
+          umma_f16_ss(slot_tmem, ad + 4u, bd + 4u, li.idesc, 1u);
+          umma_f16_ss(slot_tmem, ad + 6u, bd + 6u, li.idesc, 1u);
+        }
         umma_commit(c.bar(kBarWEmpty + ws));
         next_stage();
       }
@@ -654,6 +665,7 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
       // issued the previous chain's MMAs waits until those MMAs have read
       // their shared-memory operands, which would hold that warp back.
       const int N = layer_n(p, l);
+      bool a_in_smem = false;
       if (ok) ok = warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c);
       if (ok) {
         tc_fence_after_sync();
@@ -668,7 +680,19 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
           } else {
             uint32_t h[16];
             convert_pairs<V, 16, true>(acc, slope2, h);
-            tmem_st_x16(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
+            if (static_cast<uint32_t>(c0) < p.a_tmem_k) {
+              tmem_st_x16(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
+            } else {
+              // this row's 64 bytes of the chunk, into the 128-byte-swizzled
+              // 64-column segment of the shared-memory A buffer
+              const uint32_t kk = static_cast<uint32_t>(c0) - p.a_tmem_k;
+              const uint32_t base = a_smem + (kk >> 6) * (kTileM * 128u);
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc)
+                st_shared_v4(base + swz(row * 128u + (kk & 63u) * 2u + 16u * cc, 64), h[4 * cc],
+                             h[4 * cc + 1], h[4 * cc + 2], h[4 * cc + 3]);
+              a_in_smem = true;
+            }
           }
         }
         // (hidden widths of the narrow-precision variant are multiples of 32)
@@ -681,6 +705,8 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
           tmem_st_x8(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
         }
         if (V == kVarRowMajor) rebuild_b(l + 1);
+        // generic-proxy stores -> the next chain's MMA reads (async proxy)
+        if (a_in_smem) fence_proxy_async_smem();
         tmem_wait_st();
       }
       tc_fence_before_sync();
@@ -1377,7 +1403,7 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
   // slot the accumulator and the A region, plus one shared 32-column block
   // for the ones slab), two input stages per slot before one, two output
   // buffers before one. If the weights do not fit (fused and
-  // scalar-activation variants), stream them with at most 2 slots and the
+  // scalar-activation variants), stream them with at most 3 slots and the
   // deepest weight ring (4 down to 2 stages) that fits.
   // The narrow-precision variant: streamed weights only, on networks that
   // have E4M3 images; its A region holds four E4M3 values per column.
@@ -1391,9 +1417,25 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
     const bool streamed = mode == 1;
     if (streamed && variant == kVarRowMajor) break;
     p.a_col = acc_cols;
-    p.slot_cols = acc_cols + (((hmax / (fp8 ? 4u : 2u)) + 31u) & ~31u);
     const uint32_t max_slots = streamed ? static_cast<uint32_t>(kStreamSlots) : static_cast<uint32_t>(kMaxSlots);
     for (uint32_t slots = max_slots; slots >= 1; --slots) {
+      // A wholly in TMEM; or, for streamed FP16 weights when that leaves too
+      // few slots, its first a_tmem_k columns (a multiple of 64) in TMEM and
+      // the rest in shared memory, if every hidden width above a_tmem_k is a
+      // multiple of 64 (the shared-memory part is whole 64-column segments).
+      p.a_tmem_k = hmax;
+      p.slot_cols = acc_cols + (((hmax / (fp8 ? 4u : 2u)) + 31u) & ~31u);
+      if (slots * p.slot_cols + 32u > 512u && streamed && !fp8) {
+        const uint32_t room = (512u - 32u) / slots;
+        const uint32_t k = room > acc_cols ? ((room - acc_cols) * 2u) & ~63u : 0u;
+        bool ok = k >= 64u;
+        for (int l = 1; l < L && ok; ++l)
+          if (static_cast<uint32_t>(dims[l]) > k && dims[l] % 64 != 0) ok = false;
+        if (!ok) continue;
+        p.a_tmem_k = k;
+        p.slot_cols = acc_cols + k / 2u;
+      }
+      p.a_smem_bytes = hmax > p.a_tmem_k ? kTileM * 2u * (hmax - p.a_tmem_k) : 0u;
       const uint32_t used = slots * p.slot_cols + 32u;
       if (used > 512u) continue;
       const uint32_t groups = slots >= 3 ? 1u : 4u / slots;
@@ -1420,6 +1462,8 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
             off += 1024u;  // barrier block, keeps the input ring 1024-aligned
             p.sm_in = off;
             off += slots * depth * stage;
+            p.sm_a = off;
+            off += slots * p.a_smem_bytes;
             const uint32_t total = off + 1024u;  // + alignment slack of the dynamic smem base
             if (total <= smem_optin) {
               uint32_t cols = 32;

@@ -22,9 +22,9 @@ constexpr int kMaxBStages = kMaxSlots;       // row-major ablation: one B stage 
 constexpr int kEpiWarp0 = 8;
 constexpr int kMaxEpiWarps = 4 * kMaxSlots > 16 ? 4 * kMaxSlots : 16;
 constexpr int kMaxResidentWarps = kEpiWarp0 + kMaxEpiWarps;
-// Streamed weights: the slots' warps (16), one weight-producer warp and one
-// input-producer warp.
-constexpr int kStreamSlots = 2;    // tile slots at most with streamed weights
+// Streamed weights: the slots' warps (at most 16: 1 slot x 16, 2 x 8 or
+// 3 x 4), one weight-producer warp and one input-producer warp.
+constexpr int kStreamSlots = 3;    // tile slots at most with streamed weights
 constexpr int kOutBufs = 2;        // output staging buffers per slot (TMA-store double buffer)
 constexpr int kMaxSlabs = kMaxLayers * (kMaxDim / 16);
 constexpr uint32_t kStatusTimeout = 1u;
@@ -143,6 +143,12 @@ struct FusedParams {  // 128-byte aligned through its CUtensorMap members
   // the next layer's FP16 A (from a_col); one "ones" slab (8 columns) at
   // ones_col serves every slot's bias MMA.
   uint32_t a_col, ones_col;
+  // Streamed FP16 weights: the first a_tmem_k columns of the next layer's A
+  // sit in TMEM (from a_col), the rest -- whole 64-column segments, each
+  // 128 rows x 128 bytes with the 128-byte swizzle -- in the slot's A buffer
+  // in shared memory (sm_a + slot * a_smem_bytes), so that more tile slots
+  // fit in TMEM. a_tmem_k covers the widest hidden layer when A fits.
+  uint32_t a_tmem_k, sm_a, a_smem_bytes;
   uint32_t stream_w;    // 1: weights streamed through the ring instead of resident
   uint32_t n_wstages;   // streamed-weight ring depth
   uint32_t wstage_bytes;

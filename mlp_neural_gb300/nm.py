@@ -112,7 +112,8 @@ class Plan(ctypes.Structure):
                 ("threads", ctypes.c_int32), ("streamed_weights", ctypes.c_int32),
                 ("weight_stages", ctypes.c_int32), ("input_stages", ctypes.c_int32),
                 ("output_buffers", ctypes.c_int32), ("smem_bytes", ctypes.c_uint32),
-                ("tmem_columns", ctypes.c_uint32), ("issuing_warps", ctypes.c_int32)]
+                ("tmem_columns", ctypes.c_uint32), ("issuing_warps", ctypes.c_int32),
+                ("a_tmem_k", ctypes.c_int32)]
 
 
 GB300_SMEM_OPTIN = 232448  # opt-in shared memory per block on GB300, bytes

@@ -27,7 +27,9 @@ SMALL_DIMS = [
 # streams their weights (wide: 2 tile slots, heterogeneous: 1).
 STREAMED_DIMS = [synth.WORKLOADS["wide"].dims, synth.WORKLOADS["hetero"].dims,
                  (48, 240, 208, 176, 16),    # 1 slot; K-segments of 64, 32 and 16
-                 (80,) + (112,) * 8 + (16,)]  # 2 slots; every K leaves a tail
+                 (80,) + (112,) * 8 + (16,),  # 2 slots; every K leaves a tail
+                 (64,) + (96,) * 15 + (16,),  # 3 slots of 4 warps, 16 layers
+                 (128, 128, 64, 128, 128, 128, 128, 64, 128, 16)]  # 3 slots, A split TMEM/smem
 SENTINEL = 0x7E7E  # a NaN pattern the kernel never produces from finite data
 
 
