@@ -87,8 +87,12 @@ __host__ __device__ constexpr bool is_scalar_act(int V) {
 }
 
 __host__ __device__ constexpr bool is_stream(int V) {
-  return V == kVarFusedStream || V == kVarScalarStream || V == kVarFp8Stream;
+  return V == kVarFusedStream || V == kVarScalarStream || V == kVarFp8Stream ||
+         V == kVarFusedStreamSplitA;
 }
+
+// Part of the next layer's A may sit in shared memory (a_tmem_k, sm_a).
+__host__ __device__ constexpr bool has_split_a(int V) { return V == kVarFusedStreamSplitA; }
 
 // Layers 2..L take E4M3 operands (A: the previous layer's activations,
 // rounded as the epilogue stores them; B: the weights' E4M3 images).
@@ -474,7 +478,8 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
   const int32_t n_rounds = (c.n_local - s + S - 1) / S;  // tiles r*S + s < n_local
   const bool storer = (lane == 0) && (32 * g < n_out);
   const uint32_t b_stage = c.sbase + p.sm_b + static_cast<uint32_t>(s) * p.b_stage_bytes;
-  const uint32_t a_smem = c.sbase + p.sm_a + static_cast<uint32_t>(s) * p.a_smem_bytes;
+  const uint32_t a_smem =
+      has_split_a(V) ? c.sbase + p.sm_a + static_cast<uint32_t>(s) * p.a_smem_bytes : 0u;
 
   // Row-major ablation: this warp's share (rows wi, wi + nw, ...) of W_l
   // rebuilt in the slot's B stage, 16-byte loads, swizzled 16-byte stores.
@@ -546,7 +551,7 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
         tc_fence_after_sync();
         const uint64_t bd = desc64 + ((c.sbase + p.sm_wring + ws * p.wstage_bytes) >> 4);
         const uint32_t kj = 64u * static_cast<uint32_t>(j);
-        if (is_fp8(V) || kj < p.a_tmem_k) {
+        if (!has_split_a(V) || kj < p.a_tmem_k) {
           const uint32_t at = slot_tmem + p.a_col + (kj >> 1);
           umma_ts<is_fp8(V)>(slot_tmem, at, bd, li.idesc, j > 0 ? 1u : 0u);
           umma_ts<is_fp8(V)>(slot_tmem, at + 8u, bd + 2u, li.idesc, 1u);
@@ -665,7 +670,7 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
       // issued the previous chain's MMAs waits until those MMAs have read
       // their shared-memory operands, which would hold that warp back.
       const int N = layer_n(p, l);
-      bool a_in_smem = false;
+      bool a_in_smem = false;  // (split-A plans) a chunk went to shared memory
       if (ok) ok = warp_wait(c.bar(kBarAccFull + s), q & 1u, p, c);
       if (ok) {
         tc_fence_after_sync();
@@ -680,11 +685,12 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
           } else {
             uint32_t h[16];
             convert_pairs<V, 16, true>(acc, slope2, h);
-            if (static_cast<uint32_t>(c0) < p.a_tmem_k) {
+            if (!has_split_a(V) || static_cast<uint32_t>(c0) < p.a_tmem_k) {
               tmem_st_x16(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
             } else {
               // this row's 64 bytes of the chunk, into the 128-byte-swizzled
-              // 64-column segment of the shared-memory A buffer
+              // 64-column segment of the shared-memory A buffer (a layer
+              // wider than a_tmem_k is a multiple of 64 wide)
               const uint32_t kk = static_cast<uint32_t>(c0) - p.a_tmem_k;
               const uint32_t base = a_smem + (kk >> 6) * (kTileM * 128u);
 #pragma unroll
@@ -706,7 +712,7 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
         }
         if (V == kVarRowMajor) rebuild_b(l + 1);
         // generic-proxy stores -> the next chain's MMA reads (async proxy)
-        if (a_in_smem) fence_proxy_async_smem();
+        if (has_split_a(V) && a_in_smem) fence_proxy_async_smem();
         tmem_wait_st();
       }
       tc_fence_before_sync();
@@ -1419,13 +1425,14 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
     p.a_col = acc_cols;
     const uint32_t max_slots = streamed ? static_cast<uint32_t>(kStreamSlots) : static_cast<uint32_t>(kMaxSlots);
     for (uint32_t slots = max_slots; slots >= 1; --slots) {
-      // A wholly in TMEM; or, for streamed FP16 weights when that leaves too
-      // few slots, its first a_tmem_k columns (a multiple of 64) in TMEM and
+      // A wholly in TMEM; or, for streamed FP16 weights (fused kernel) when
+      // that leaves too few slots, its first a_tmem_k columns (a multiple of 64) in TMEM and
       // the rest in shared memory, if every hidden width above a_tmem_k is a
       // multiple of 64 (the shared-memory part is whole 64-column segments).
       p.a_tmem_k = hmax;
       p.slot_cols = acc_cols + (((hmax / (fp8 ? 4u : 2u)) + 31u) & ~31u);
-      if (slots * p.slot_cols + 32u > 512u && streamed && !fp8) {
+      if (slots * p.slot_cols + 32u > 512u && streamed &&
+          (variant == kVarFused || variant == kVarPaired)) {
         const uint32_t room = (512u - 32u) / slots;
         const uint32_t k = room > acc_cols ? ((room - acc_cols) * 2u) & ~63u : 0u;
         bool ok = k >= 64u;
@@ -1554,7 +1561,8 @@ cudaError_t launch_fused(const FusedParams& p, int variant, int grid, uint32_t s
                          cudaStream_t stream, bool overlap) {
   if (p.stream_w) {
     if (variant == kVarFused || variant == kVarPaired)
-      return launch_variant<kVarFusedStream>(p, grid, smem, stream, overlap);
+      return p.a_smem_bytes ? launch_variant<kVarFusedStreamSplitA>(p, grid, smem, stream, overlap)
+                            : launch_variant<kVarFusedStream>(p, grid, smem, stream, overlap);
     if (variant == kVarScalar) return launch_variant<kVarScalarStream>(p, grid, smem, stream, overlap);
     if (variant == kVarFp8) return launch_variant<kVarFp8Stream>(p, grid, smem, stream, overlap);
     return cudaErrorInvalidValue;

@@ -31,10 +31,12 @@ constexpr uint32_t kStatusTimeout = 1u;
 
 // Public variants 0..4 (nm_variant); 8 and 9 are the fused and the
 // scalar-activation kernels with streamed instead of resident weights, chosen
-// by the planner when the packed weights do not fit in shared memory; 10 is
-// the narrow-precision variant, which always streams its weights. The
-// paired-tiles variant runs the fused kernel with a plan that issues the tile
-// regions two at a time.
+// by the planner when the packed weights do not fit in shared memory; 11 is
+// the fused streamed kernel for plans that keep part of A in shared memory
+// (its own instantiation, so the other streamed plans run code without those
+// branches); 10 is the narrow-precision variant, which always streams its
+// weights. The paired-tiles variant runs the fused kernel with a plan that
+// issues the tile regions two at a time.
 enum Variant : int {
   kVarFused = 0,
   kVarRowMajor = 1,
@@ -43,7 +45,8 @@ enum Variant : int {
   kVarFp8 = 4,
   kVarFusedStream = 8,
   kVarScalarStream = 9,
-  kVarFp8Stream = 10
+  kVarFp8Stream = 10,
+  kVarFusedStreamSplitA = 11
 };
 constexpr int kMaxWStages = 4;     // streamed-weight ring depth (upper bound)
 
