@@ -136,21 +136,24 @@ nm_status nm_mlp_packed_size(const nm_mlp *h, size_t *bytes);
  * W: host array of L device pointers; W[l] is FP16 [dims[l+1]][dims[l]]
  *    row-major (row o holds the weights of output o).
  * b: host array of L device pointers; b[l] is FP16 [dims[l+1]].
- * The packed bits are a permutation of the input bits (no arithmetic). For
- * a network that has E4M3 images (nm_mlp_packed_fp8) the call also writes
- * those, rounding every weight of W_2 .. W_L to E4M3.
+ * The packed bits are a permutation of the input bits (no arithmetic). When
+ * the handle's variant is NM_VARIANT_FP8_WEIGHTS the call also writes the
+ * E4M3 images (nm_mlp_packed_fp8), rounding every weight of W_2 .. W_L to
+ * E4M3; otherwise the first dispatch of that variant writes them, from the
+ * packed blob, on its own stream.
  * Errors: NM_ERR_INVALID_ARG (NULL or misaligned pointer), NM_ERR_CUDA. */
 nm_status nm_mlp_pack_weights(nm_mlp *h, const void *const *W, const void *const *b,
                               nm_stream stream);
 
-/* The E4M3 weight images of NM_VARIANT_FP8_WEIGHTS, which nm_mlp_pack_weights
- * writes beside the packed blob (same allocation, owned by the handle):
- * device address and size in bytes (read-only; for byte-for-byte checks).
+/* The E4M3 weight images of NM_VARIANT_FP8_WEIGHTS, kept beside the packed
+ * blob (same allocation, owned by the handle): device address and size in
+ * bytes (read-only; for byte-for-byte checks).
  * Layout: the images of W_2 .. W_L in order, each starting at a multiple of
  * 1024 bytes; an image's k range is cut into 128-, then 64-, then 32-column
  * segments (1024-aligned, N rows of w bytes, 128/64/32-byte swizzle).
  * Errors: NM_ERR_INVALID_ARG, NM_ERR_UNSUPPORTED (the network has no such
- * images: L < 2 or a hidden width not a multiple of 32). */
+ * images: L < 2 or a hidden width not a multiple of 32), NM_ERR_NOT_PACKED
+ * (not written since the last pack: see nm_mlp_pack_weights). */
 nm_status nm_mlp_packed_fp8(const nm_mlp *h, const void **region, size_t *bytes);
 
 /* Inverse of nm_mlp_pack_weights, into caller buffers of the same shapes.

@@ -69,9 +69,9 @@ cudaError_t launch_pack(const PackParams& p, bool unpack, int num_sms, cudaStrea
 }
 
 // E4M3 images: thread g rounds the 16 FP16 weights W_l[n][col .. col + 15]
-// (two 16-byte loads of one row) to E4M3 and stores them as one 16-byte
-// chunk. In the FP16-unit view of the image (K/2 columns of 2 bytes), the
-// chunk is the 8-column chunk at column col / 2.
+// -- two 16-byte chunks of the packed FP16 image -- to E4M3 and stores them
+// as one 16-byte chunk. In the FP16-unit view of the E4M3 image (K/2 columns
+// of 2 bytes), that chunk is the 8-column chunk at column col / 2.
 __global__ void __launch_bounds__(256) pack_fp8_kernel(const __grid_constant__ PackParams p,
                                                        const __grid_constant__ Fp8Offsets o,
                                                        uint8_t* region) {
@@ -87,8 +87,13 @@ __global__ void __launch_bounds__(256) pack_fp8_kernel(const __grid_constant__ P
     int w, k0;
     locate(static_cast<uint32_t>(N), K >> 1, col >> 1, off, w, k0);
     const uint32_t dst = o.off[l] + off + swz(static_cast<uint32_t>(n * 2 * w + (col - 2 * k0)), w);
-    const uint4* src = reinterpret_cast<const uint4*>(p.rm_w[l] + static_cast<size_t>(n) * K + col);
-    const uint4 a = __ldg(src), b = __ldg(src + 1);
+    // the two source chunks (columns col and col + 8 lie in one FP16 segment)
+    locate(static_cast<uint32_t>(N), K, col, off, w, k0);
+    const uint32_t src = p.w_off[l] + off + swz(static_cast<uint32_t>(n * 2 * w + (col - k0) * 2), w);
+    const uint32_t src2 =
+        p.w_off[l] + off + swz(static_cast<uint32_t>(n * 2 * w + (col + 8 - k0) * 2), w);
+    const uint4 a = *reinterpret_cast<const uint4*>(p.blob + src);
+    const uint4 b = *reinterpret_cast<const uint4*>(p.blob + src2);
     const uint32_t hw[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     uint32_t q[4];
 #pragma unroll
@@ -289,6 +294,7 @@ struct nm_mlp {
   size_t fp8_size = 0;
   uint32_t fp8_off[nm::kMaxLayers] = {};
   uint8_t* sched8 = nullptr;
+  bool fp8_valid = false;  // the images match the packed FP16 blob
   bool packed = false;
   bool mirror_valid = false;
   // A packing kernel (weights or the row-major mirror) was the last of this
@@ -359,6 +365,19 @@ nm_status cached_io_maps(nm_mlp* h, const void* in, void* out, int64_t n) {
 
 PackParams make_pack_params(const nm_mlp* h) {
   return nm::make_pack_params(h->dims, h->L, h->w_off, h->params.bias_off, h->blob);
+}
+
+// The E4M3 images, converted from the packed FP16 blob on `stream` the first
+// time the narrow-precision variant needs them after a pack.
+nm_status ensure_fp8(nm_mlp* h, cudaStream_t stream) {
+  if (h->fp8_valid) return NM_OK;
+  if (nm::launch_pack_fp8(make_pack_params(h), h->fp8_off, h->blob + h->fp8_base, h->num_sms,
+                          stream) != cudaSuccess)
+    return NM_ERR_CUDA;
+  h->pack_pending = true;
+  h->pack_stream = stream;
+  h->fp8_valid = true;
+  return NM_OK;
 }
 
 nm_status ensure_mirror(nm_mlp* h, cudaStream_t stream) {
@@ -598,6 +617,7 @@ nm_status nm_mlp_packed_blob(const nm_mlp* h, const void** blob) {
 nm_status nm_mlp_packed_fp8(const nm_mlp* h, const void** region, size_t* bytes) {
   if (!h || !region || !bytes) return NM_ERR_INVALID_ARG;
   if (!h->fp8_size) return NM_ERR_UNSUPPORTED;
+  if (!h->packed || !h->fp8_valid) return NM_ERR_NOT_PACKED;
   *region = h->blob + h->fp8_base;
   *bytes = h->fp8_size;
   return NM_OK;
@@ -614,10 +634,11 @@ nm_status nm_mlp_pack_weights(nm_mlp* h, const void* const* W, const void* const
   }
   if (nm::launch_pack(pp, false, h->num_sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return NM_ERR_CUDA;
-  if (h->fp8_size &&
-      nm::launch_pack_fp8(pp, h->fp8_off, h->blob + h->fp8_base, h->num_sms,
-                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return NM_ERR_CUDA;
+  h->fp8_valid = false;
+  if (h->variant == nm::kVarFp8) {
+    const nm_status st = ensure_fp8(h, reinterpret_cast<cudaStream_t>(stream));
+    if (st != NM_OK) return st;
+  }
   h->packed = true;
   h->mirror_valid = false;
   h->pack_pending = true;
@@ -650,6 +671,10 @@ nm_status nm_mlp_infer(nm_mlp* h, const void* in, int64_t n, void* out, nm_strea
     const nm_status st = ensure_mirror(h, s);
     if (st != NM_OK) return st;
   }
+  if (h->variant == nm::kVarFp8) {
+    const nm_status st = ensure_fp8(h, s);
+    if (st != NM_OK) return st;
+  }
   return launch_infer(h, in, n, out, s);
 }
 
@@ -663,6 +688,10 @@ nm_status nm_mlp_infer_host(nm_mlp* h, const void* host_in, int64_t n, void* hos
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (h->variant == nm::kVarRowMajor) {
     const nm_status st = ensure_mirror(h, s);
+    if (st != NM_OK) return st;
+  }
+  if (h->variant == nm::kVarFp8) {
+    const nm_status st = ensure_fp8(h, s);
     if (st != NM_OK) return st;
   }
   nm_status st = ensure_host_pipeline(h);

@@ -197,9 +197,9 @@ struct PackParams {
 
 cudaError_t launch_pack(const PackParams& p, bool unpack, int num_sms, cudaStream_t stream);
 
-// Writes the E4M3 images (fp8_layout) of W_1..W_{L-1} from the row-major
-// FP16 weights p.rm_w into `region`: each thread rounds 16 weights of one row
-// (round to nearest even, saturating at 448) and stores them as one swizzled
+// Writes the E4M3 images (fp8_layout) of W_1..W_{L-1} from the packed FP16
+// blob p.blob into `region`: each thread rounds 16 weights of one row (round
+// to nearest even, saturating at 448) and stores them as one swizzled
 // 16-byte chunk.
 cudaError_t launch_pack_fp8(const PackParams& p, const uint32_t* fp8_off, uint8_t* region,
                             int num_sms, cudaStream_t stream);

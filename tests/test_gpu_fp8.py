@@ -68,14 +68,29 @@ def fp8_compare(gpu16, cpu16, what=""):
 
 @pytest.mark.parametrize("dims", FP8_DIMS)
 def test_fp8_images_bit_exact(orc, dims):
-    W, b, _ = synth.small_net_inputs(dims, seed=31, n=1)
-    m = make_net(dims, W, b)
-    ptr, size = m.packed_fp8()
+    """The E4M3 images, written from the packed FP16 blob by the first
+    dispatch of the variant after a pack, or by a pack made with the variant
+    already selected."""
+    import torch
+    lib = nm()
+    W, b, x = synth.small_net_inputs(dims, seed=31, n=3)
     ref = orc.pack_fp8(dims, W)
+    m = make_net(dims, W, b)
+    with pytest.raises(lib.NmError) as e:
+        m.packed_fp8()
+    assert e.value.status == lib.NM_ERR_NOT_PACKED
+    _infer(m, x)
+    ptr, size = m.packed_fp8()
     assert size == ref.size
     assert np.array_equal(read_device(ptr, size), ref)
     # the FP16 blob is unchanged by the extra images
     assert np.array_equal(read_device(m.packed_blob(), m.packed_size()), orc.pack(dims, W, b))
+    m2 = lib.MLP(dims)
+    m2.set_variant(lib.NM_VARIANT_FP8_WEIGHTS)
+    m2.pack_weights([to_dev(w) for w in W], [to_dev(v) for v in b])
+    torch.cuda.synchronize()
+    ptr2, _ = m2.packed_fp8()
+    assert np.array_equal(read_device(ptr2, size), ref)
 
 
 @pytest.mark.parametrize("dims", FP8_DIMS[:4])
