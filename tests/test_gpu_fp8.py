@@ -156,3 +156,24 @@ def test_fp8_variant_needs_e4m3_images():
     with pytest.raises(lib.NmError) as e:
         m.packed_fp8()
     assert e.value.status == lib.NM_ERR_UNSUPPORTED
+
+
+def test_fp8_host_buffer_path_bit_identical():
+    """nm_mlp_infer_host with the narrow-precision variant selected right
+    after an FP16 pack: the host-buffer call writes the E4M3 images itself
+    (on the caller's stream, before its chunks) and matches nm_mlp_infer."""
+    import torch
+    lib = nm()
+    dims = synth.WORKLOADS["wide"].dims
+    W, b, x = synth.small_net_inputs(dims, seed=77, n=3000)
+    m = make_net(dims, W, b)
+    m.set_variant(lib.NM_VARIANT_FP8_WEIGHTS)
+    m.set_host_chunk(1024)
+    xh = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.float16).pin_memory()
+    out = torch.empty((x.shape[0], dims[-1]), dtype=torch.float16).pin_memory()
+    m.infer_host(xh, out)
+    torch.cuda.synchronize()
+    assert m.device_status() == lib.NM_OK
+    y_host = out.view(torch.int16).numpy().view(np.uint16).copy()
+    y_dev = _infer(m, x)
+    assert np.array_equal(y_host, y_dev)
