@@ -80,6 +80,42 @@ def assert_close(gpu16: np.ndarray, cpu16: np.ndarray, what=""):
     return float(err.max()) if err.size else 0.0
 
 
+def fp8_rows_parallel(orc, dims, W, b, x, y_gpu, row_frac, tol_abs, tol_rel, chunk=32768,
+                      threads=None):
+    """Every row of y_gpu against the oracle's E4M3 pass on all host cores
+    (as check_rows_parallel): at most row_frac of the rows may differ at all,
+    and no element by more than tol_abs + tol_rel |cpu|. Returns (rows
+    checked, rows that differ, largest |gpu - cpu|, threads used)."""
+    from concurrent.futures import ThreadPoolExecutor
+    n = x.shape[0]
+    assert y_gpu.shape == (n, dims[-1])
+    if threads is None:
+        threads = os.cpu_count() or 1
+
+    def work(r0):
+        r1 = min(n, r0 + chunk)
+        ref = orc.forward_fp8(dims, W, b, x[r0:r1]).view(np.float16).astype(np.float64)
+        got = y_gpu[r0:r1].view(np.float16).astype(np.float64)
+        err = np.abs(got - ref)
+        badm = ~(err <= tol_abs + tol_rel * np.abs(ref))
+        first = None
+        if badm.any():
+            i, j = np.argwhere(badm)[0]
+            first = (r0 + int(i), int(j), float(got[i, j]), float(ref[i, j]))
+        return (int((err.max(axis=1) > 0).sum()), int(badm.sum()),
+                float(np.nanmax(err)) if err.size else 0.0, first)
+
+    with ThreadPoolExecutor(threads) as ex:
+        res = list(ex.map(work, range(0, n, chunk)))
+    rows = sum(r[0] for r in res)
+    bad = sum(r[1] for r in res)
+    firsts = [r[3] for r in res if r[3] is not None]
+    assert bad == 0, (f"{bad} elements outside |gpu-cpu| <= {tol_abs} + {tol_rel}|cpu|; "
+                      f"first (row, col, gpu, cpu) = {firsts[0]}")
+    assert rows <= row_frac * n, f"{rows} of {n} rows differ from the oracle"
+    return n, rows, max(r[2] for r in res), threads
+
+
 def check_rows_parallel(orc, dims, W, b, x, y_gpu, chunk=32768, threads=None):
     """Every row of y_gpu (uint16 FP16 bits, [n, d_L]) against the oracle on
     the same inputs, within |gpu - cpu| <= 1e-2 + 1e-2|cpu| per element.
