@@ -971,10 +971,12 @@ __device__ __forceinline__ void run_issuer(const FusedParams& p, const Ctx& c, i
           if (nt > 1) fire_ts(ip, s0 + 1);
         }
         // ... then, while their epilogue runs, the next chain's descriptors
-        // (layers after the first), and the barrier after that epilogue.
+        // (layers after the first), and the barrier after that epilogue. The
+        // warp is not reconverged after the elected lane's issue: its other
+        // lanes go ahead, so the barrier is the per-thread form.
         if (l + 1 < L) ip = prep_ts(l + 1);
         tc_fence_before_sync();
-        named_bar_sync(bar_id, bar_threads);
+        named_bar_sync_lanes(bar_id, bar_threads);
       }
     }
   }

@@ -83,6 +83,12 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// The same barrier for a warp whose lanes may arrive at different times (the
+// non-.aligned form: every thread arrives on its own, `count` counts threads).
+__device__ __forceinline__ void named_bar_sync_lanes(uint32_t id, uint32_t count) {
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Explicit shared-memory loads (the address is a shared-window address).
 __device__ __forceinline__ float4 ld_shared_f32x4(uint32_t addr) {
   float4 v;
