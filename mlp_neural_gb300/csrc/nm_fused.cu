@@ -4,25 +4,30 @@
 // and runs every layer of the network on each tile without leaving the SM
 // ("Optimization Techniques: Squeezing the Silicon", "Kernel Fusion": one
 // write to memory, intermediates stay on chip). Up to five tiles are in
-// flight per CTA (tile slots; TMEM decides how many). A slot owns a TMEM
-// region holding its FP32 accumulator and, beside it, the FP16 activations
-// that feed the next layer as the tensor core's A operand; the input tile
-// (layer 1's A), the weights, the bias operands and the output staging live in
-// shared memory. Roles, by warp:
-//   slot warps   4 x G per slot (the 4 TMEM lane quadrants x G column
+// flight per CTA with resident weights, three with streamed ones (tile
+// slots; TMEM decides how many). A slot owns a TMEM region holding its FP32
+// accumulator and, beside it, the activations that feed the next layer as
+// the tensor core's A operand (FP16 pairs; E4M3 quads in the narrow-precision
+// variant; a streamed plan may keep the upper 64-column segments of A in
+// shared memory instead, to fit one more slot). The input tile (layer 1's A),
+// the weights, the bias operands and the output staging live in shared
+// memory. Roles, by warp:
+//   epilogue warps  4 x G per slot (the 4 TMEM lane quadrants x G column
 //                groups). Per layer they wait for the accumulator, read it
 //                (tcgen05.ld), round to FP16, apply max(h, h*half(0.01)) and
-//                write the pairs as the next layer's A (tcgen05.st) -- or,
-//                after the last layer, into an output staging tile each warp
-//                sends out by TMA -- then meet at the slot's named barrier.
-//                One lane of them, chosen by elect.sync, then issues the next
-//                layer's tcgen05.mma chain, D[128 x N] (FP32, TMEM) =
-//                A[128 x K] * W^T + b, and commits it to the slot's
-//                accumulator barrier. With streamed weights that lane also
-//                takes each K-segment from the weight ring.
+//                write the result as the next layer's A -- or, after the last
+//                layer, into an output staging tile each warp sends out by
+//                TMA -- then meet at the slot's named barrier.
+//   issuing lane  one elect.sync lane issues each layer's tcgen05.mma chain,
+//                D[128 x N] (FP32, TMEM) = A[128 x K] * W^T + b, and commits
+//                it to the slot's accumulator barrier: with resident weights
+//                a dedicated warp per slot (it prepares the next chain's
+//                descriptors while the epilogue runs); with streamed weights
+//                a lane of one of the slot's epilogue warps, which also takes
+//                each K-segment from the weight ring.
 //   weight producer (streamed weights only): copies the layers' K-segments
 //                into the shared weight ring.
-//   input producer (last warp): keeps every slot's input ring filled by TMA.
+//   input producer: keeps every slot's input ring filled by TMA.
 //
 // The page "Profiling neural material inference" fixes the arithmetic
 // ("Experiment setup": the full layer chain per evaluation; "Bad versus good
@@ -37,10 +42,10 @@
 // descriptors follow from the ring stage it sits in, and its four MMAs are
 // issued straight-line too.
 //
-// Dispatches overlap on a stream: each CTA lets the next kernel be scheduled
-// as soon as it starts (programmatic dependent launch), and every thread
-// waits on the grid dependency before touching inputs, outputs or the status
-// word, so only the prologue runs alongside the previous kernel.
+// Dispatches overlap on a stream: once a CTA holds its tensor memory it lets
+// the next kernel be scheduled (programmatic dependent launch), and every
+// thread waits on the grid dependency before touching inputs, outputs or the
+// status word, so only the prologue runs alongside the previous kernel.
 //
 // Every wait is bounded by a wall-clock limit. A wait that gives up sets the
 // device status word and a CTA-wide abort flag; every role then stops, waits
@@ -1428,9 +1433,9 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
     const uint32_t max_slots = streamed ? static_cast<uint32_t>(kStreamSlots) : static_cast<uint32_t>(kMaxSlots);
     for (uint32_t slots = max_slots; slots >= 1; --slots) {
       // A wholly in TMEM; or, for streamed FP16 weights (fused kernel) when
-      // that leaves too few slots, its first a_tmem_k columns (a multiple of 64) in TMEM and
-      // the rest in shared memory, if every hidden width above a_tmem_k is a
-      // multiple of 64 (the shared-memory part is whole 64-column segments).
+      // that leaves too few slots, its first a_tmem_k columns (a multiple of
+      // 64) in TMEM and the rest in shared memory, if every hidden width
+      // above a_tmem_k is a multiple of 64 (whole 64-column segments).
       p.a_tmem_k = hmax;
       p.slot_cols = acc_cols + (((hmax / (fp8 ? 4u : 2u)) + 31u) & ~31u);
       if (slots * p.slot_cols + 32u > 512u && streamed &&
