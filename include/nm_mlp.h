@@ -140,7 +140,8 @@ nm_status nm_mlp_packed_size(const nm_mlp *h, size_t *bytes);
  * the handle's variant is NM_VARIANT_FP8_WEIGHTS the call also writes the
  * E4M3 images (nm_mlp_packed_fp8), rounding every weight of W_2 .. W_L to
  * E4M3; otherwise the first dispatch of that variant writes them, from the
- * packed blob, on its own stream.
+ * packed blob, on its own stream (that first dispatch cannot be captured
+ * into a CUDA graph: see nm_mlp_infer).
  * Errors: NM_ERR_INVALID_ARG (NULL or misaligned pointer), NM_ERR_CUDA. */
 nm_status nm_mlp_pack_weights(nm_mlp *h, const void *const *W, const void *const *b,
                               nm_stream stream);
@@ -172,6 +173,11 @@ nm_status nm_mlp_packed_blob(const nm_mlp *h, const void **blob);
  * NM_ERR_NOT_PACKED, NM_ERR_UNSUPPORTED (the network does not fit the
  * selected variant's shared-memory budget), NM_ERR_CUDA (launch failure).
  * A kernel-side wait that gives up is reported by nm_mlp_device_status.
+ * The first dispatch of the row-major variant, and of the narrow-precision
+ * variant after a pack made with another variant selected, first converts
+ * the weights once (a row-major copy, or the E4M3 images); it returns
+ * NM_ERR_UNSUPPORTED, before enqueuing anything, if `stream` is being
+ * captured into a CUDA graph (make one such dispatch before capturing).
  * Stream order: the dispatch is launched with programmatic stream
  * serialisation. Its set-up (barriers, tensor memory, weight staging) may
  * run while the previous kernel on `stream` finishes. It reads `in` and

@@ -369,8 +369,17 @@ PackParams make_pack_params(const nm_mlp* h) {
 
 // The E4M3 images, converted from the packed FP16 blob on `stream` the first
 // time the narrow-precision variant needs them after a pack.
+// A one-time conversion the caller did not ask for must not end up only in a
+// graph being captured (the handle would count it as done before any replay):
+// such a dispatch is refused while `stream` captures.
+bool capturing(cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  return cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone;
+}
+
 nm_status ensure_fp8(nm_mlp* h, cudaStream_t stream) {
   if (h->fp8_valid) return NM_OK;
+  if (capturing(stream)) return NM_ERR_UNSUPPORTED;
   if (nm::launch_pack_fp8(make_pack_params(h), h->fp8_off, h->blob + h->fp8_base, h->num_sms,
                           stream) != cudaSuccess)
     return NM_ERR_CUDA;
@@ -382,6 +391,7 @@ nm_status ensure_fp8(nm_mlp* h, cudaStream_t stream) {
 
 nm_status ensure_mirror(nm_mlp* h, cudaStream_t stream) {
   if (h->mirror_valid) return NM_OK;
+  if (capturing(stream)) return NM_ERR_UNSUPPORTED;
   if (!h->mirror) {
     if (cudaMalloc(&h->mirror, h->mirror_elems * sizeof(uint16_t)) != cudaSuccess) {
       h->mirror = nullptr;

@@ -176,3 +176,47 @@ def test_fp8_host_buffer_path_bit_identical():
     y_host = out.view(torch.int16).numpy().view(np.uint16).copy()
     y_dev = _infer(m, x)
     assert np.array_equal(y_host, y_dev)
+
+
+@pytest.mark.parametrize("variant_name", ["NM_VARIANT_FP8_WEIGHTS", "NM_VARIANT_ROWMAJOR_WEIGHTS"])
+def test_one_time_conversion_refused_inside_a_capture(orc, variant_name):
+    """The first dispatch of a variant that converts the weights once (E4M3
+    images, row-major copy) is refused while its stream is captured -- the
+    handle would count the conversion as done before any replay -- and a
+    capture made after one eager dispatch replays correctly."""
+    import torch
+    lib = nm()
+    v = getattr(lib, variant_name)
+    dims = (64, 128, 128, 16)
+    n = 700
+    W, b, x1 = synth.small_net_inputs(dims, seed=41, n=n)
+    _, _, x2 = synth.small_net_inputs(dims, seed=42, n=n)
+    fwd = orc.forward_fp8 if v == lib.NM_VARIANT_FP8_WEIGHTS else orc.forward
+    m = make_net(dims, W, b)
+    m.set_variant(v)
+    xd = to_dev(x1)
+    od = torch.empty((n, dims[-1]), dtype=torch.float16, device="cuda")
+    side = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    status = []
+    with torch.cuda.graph(g, stream=side):
+        status.append(m.infer_raw(xd.data_ptr(), n, od.data_ptr(), side))
+    assert status == [lib.NM_ERR_UNSUPPORTED]
+    m.infer(xd, od)  # eager: converts once
+    torch.cuda.synchronize()
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=side):
+        m.infer(xd, od, stream=side)
+    for x in (x1, x2):
+        xd.copy_(to_dev(x))
+        od.fill_(float("nan"))
+        g2.replay()
+        torch.cuda.synchronize()
+        y = to_host(od)
+        if v == lib.NM_VARIANT_FP8_WEIGHTS:
+            fp8_compare(y, fwd(dims, W, b, x))
+        else:
+            from gpu_util import assert_close
+            assert_close(y, fwd(dims, W, b, x))
+    assert m.device_status() == lib.NM_OK
+    m.close()
