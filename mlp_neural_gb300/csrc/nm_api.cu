@@ -377,9 +377,9 @@ bool capturing(cudaStream_t stream) {
   return cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone;
 }
 
-nm_status ensure_fp8(nm_mlp* h, cudaStream_t stream) {
+nm_status ensure_fp8(nm_mlp* h, cudaStream_t stream, bool in_pack = false) {
   if (h->fp8_valid) return NM_OK;
-  if (capturing(stream)) return NM_ERR_UNSUPPORTED;
+  if (!in_pack && capturing(stream)) return NM_ERR_UNSUPPORTED;
   if (nm::launch_pack_fp8(make_pack_params(h), h->fp8_off, h->blob + h->fp8_base, h->num_sms,
                           stream) != cudaSuccess)
     return NM_ERR_CUDA;
@@ -646,7 +646,8 @@ nm_status nm_mlp_pack_weights(nm_mlp* h, const void* const* W, const void* const
     return NM_ERR_CUDA;
   h->fp8_valid = false;
   if (h->variant == nm::kVarFp8) {
-    const nm_status st = ensure_fp8(h, reinterpret_cast<cudaStream_t>(stream));
+    // part of the pack the caller asked for: captured with it if it is
+    const nm_status st = ensure_fp8(h, reinterpret_cast<cudaStream_t>(stream), true);
     if (st != NM_OK) return st;
   }
   h->packed = true;

@@ -220,3 +220,26 @@ def test_one_time_conversion_refused_inside_a_capture(orc, variant_name):
             assert_close(y, fwd(dims, W, b, x))
     assert m.device_status() == lib.NM_OK
     m.close()
+
+
+def test_pack_with_fp8_selected_can_be_captured(orc):
+    """A pack made with the E4M3 variant selected writes the images as part
+    of the pack, so it can be captured and replayed like any pack."""
+    import torch
+    lib = nm()
+    dims = synth.WORKLOADS["wide"].dims
+    W, b, x = synth.small_net_inputs(dims, seed=43, n=300)
+    m = lib.MLP(dims)
+    m.set_variant(lib.NM_VARIANT_FP8_WEIGHTS)
+    Wd = [to_dev(w) for w in W]
+    bd = [to_dev(v) for v in b]
+    side = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        m.pack_weights(Wd, bd, side)
+    g.replay()
+    torch.cuda.synchronize()
+    ptr, size = m.packed_fp8()
+    assert np.array_equal(read_device(ptr, size), orc.pack_fp8(dims, W))
+    fp8_compare(_infer(m, x), orc.forward_fp8(dims, W, b, x))
+    m.close()
