@@ -66,7 +66,8 @@ typedef enum nm_status {
     NM_ERR_NOT_PACKED = 3,   /* infer or unpack before nm_mlp_pack_weights */
     NM_ERR_OOM = 4,          /* device allocation failed */
     NM_ERR_CUDA = 5,         /* a CUDA runtime/driver call or launch failed */
-    NM_ERR_TIMEOUT = 6       /* a bounded wait inside a kernel gave up (see nm_mlp_device_status) */
+    NM_ERR_TIMEOUT = 6,      /* a bounded wait inside a kernel gave up (see nm_mlp_device_status) */
+    NM_ERR_RANGE_CHECK = 7   /* checking build only: a kernel-side range check failed */
 } nm_status;
 
 /* Kernel variants. NM_VARIANT_FUSED is the product path; the row-major and
@@ -222,9 +223,11 @@ nm_status nm_mlp_set_host_chunk(nm_mlp *h, int64_t rows);
 nm_status nm_mlp_set_variant(nm_mlp *h, nm_variant v);
 
 /* Synchronise `stream`, then read and clear the handle's device status word.
- * Returns NM_ERR_TIMEOUT if any kernel of this handle gave up a bounded wait
- * since the last call (its outputs are then undefined), NM_ERR_CUDA if the
- * synchronisation reported an error, else NM_OK. */
+ * Returns NM_ERR_RANGE_CHECK if (checking build) a kernel of this handle
+ * found an address outside its plan's tensor or shared memory,
+ * NM_ERR_TIMEOUT if one gave up a bounded wait since the last call (its
+ * outputs are then undefined), NM_ERR_CUDA if the synchronisation reported an
+ * error, else NM_OK. */
 nm_status nm_mlp_device_status(nm_mlp *h, nm_stream stream);
 
 /* Limit, in nanoseconds, of every wait inside the inference kernels
@@ -239,6 +242,25 @@ nm_status nm_mlp_set_wait_limit(nm_mlp *h, uint64_t nanoseconds);
  * give-up path (status word set, copies drained, tensor memory freed) without
  * any fault. The outputs of such a launch are undefined. */
 nm_status nm_mlp_set_test_stall(nm_mlp *h, int32_t enable);
+
+/* The checking build. The library can be compiled with NM_RANGE_CHECKS
+ * defined (libnmmlp_check.so; `python -m mlp_neural_gb300.build --checked`):
+ * its kernels then compare every tensor-memory column range they load,
+ * store or accumulate into (against the columns the plan uses), and every
+ * shared-memory range a copy or store writes (against the end of the plan's
+ * shared-memory layout, and each copy against its buffer), and record a
+ * miss in the status word, reported by nm_mlp_device_status as
+ * NM_ERR_RANGE_CHECK, without changing what they access: a stand-in for a
+ * memory checker over the memories such a tool does not see.
+ * nm_checking_build returns 1 in that build, 0 otherwise. */
+int32_t nm_checking_build(void);
+
+/* Test hook of the checking build: compare tensor-memory columns with
+ * `tmem_columns` instead of the plan's (0 restores the plan's; a limit above
+ * the plan's is ignored), so that a test can see a check fire without any
+ * access changing. No effect in the normal build. Errors:
+ * NM_ERR_INVALID_ARG (null handle). */
+nm_status nm_mlp_set_test_check_limit(nm_mlp *h, uint32_t tmem_columns);
 
 /* Inference that allocates no device memory. The source pages have no
  * counterpart to this call; it exists for callers that cannot call

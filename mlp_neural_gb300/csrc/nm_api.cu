@@ -306,6 +306,7 @@ struct nm_mlp {
   int variant = nm::kVarFused;
   uint64_t wait_ns = 2000000000ull;
   uint32_t test_stall = 0;
+  uint32_t test_check_cols = 0;  // checking build: lowered TMEM limit (0: none)
   int device = 0;
   int num_sms = 0;
   uint32_t smem_optin = 0;
@@ -424,6 +425,7 @@ nm_status launch_infer(nm_mlp* h, const void* in, int64_t n, void* out, cudaStre
   p.test_stall = h->test_stall;
   const uint32_t smem = nm::plan_fused_smem(p, h->dims, h->variant, h->smem_optin);
   if (smem == 0) return NM_ERR_UNSUPPORTED;
+  if (h->test_check_cols && h->test_check_cols < p.chk_tmem_cols) p.chk_tmem_cols = h->test_check_cols;
   const int grid = p.num_tiles < h->num_sms ? p.num_tiles : h->num_sms;
   const bool after_pack = h->pack_pending && s == h->pack_stream;
   if (nm::launch_fused(p, h->variant, grid, smem, s, !after_pack) != cudaSuccess) return NM_ERR_CUDA;
@@ -481,7 +483,7 @@ nm_status ensure_host_pipeline(nm_mlp* h) {
 
 extern "C" {
 
-int32_t nm_abi_version(void) { return 3; }
+int32_t nm_abi_version(void) { return 4; }
 
 const char* nm_status_str(nm_status s) {
   switch (s) {
@@ -492,6 +494,7 @@ const char* nm_status_str(nm_status s) {
     case NM_ERR_OOM: return "NM_ERR_OOM";
     case NM_ERR_CUDA: return "NM_ERR_CUDA";
     case NM_ERR_TIMEOUT: return "NM_ERR_TIMEOUT";
+    case NM_ERR_RANGE_CHECK: return "NM_ERR_RANGE_CHECK";
   }
   return "NM_ERR_UNKNOWN";
 }
@@ -765,7 +768,7 @@ nm_status nm_mlp_device_status(nm_mlp* h, nm_stream stream) {
   if (cudaMemcpy(&v, h->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return NM_ERR_CUDA;
   if (v != 0) {
     if (cudaMemset(h->status, 0, sizeof(uint32_t)) != cudaSuccess) return NM_ERR_CUDA;
-    return NM_ERR_TIMEOUT;
+    return (v & nm::kStatusRangeCheck) ? NM_ERR_RANGE_CHECK : NM_ERR_TIMEOUT;
   }
   return NM_OK;
 }
@@ -780,6 +783,20 @@ nm_status nm_mlp_set_test_stall(nm_mlp* h, int32_t enable) {
   if (!h) return NM_ERR_INVALID_ARG;
   h->test_stall = enable ? 1u : 0u;
   return NM_OK;
+}
+
+nm_status nm_mlp_set_test_check_limit(nm_mlp* h, uint32_t tmem_columns) {
+  if (!h) return NM_ERR_INVALID_ARG;
+  h->test_check_cols = tmem_columns;
+  return NM_OK;
+}
+
+int32_t nm_checking_build(void) {
+#ifdef NM_RANGE_CHECKS
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 void nm_mlp_destroy(nm_mlp* h) {

@@ -135,6 +135,60 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// The checking build (NM_RANGE_CHECKS): every tensor-memory column range a
+// warp loads, stores or accumulates into, and every shared-memory range a
+// copy or store writes, is compared with the plan's limits before the access;
+// a range outside them sets kStatusRangeCheck in the status word (the access
+// itself is unchanged). In the normal build these compile to nothing.
+//
+// Tensor memory: the columns [addr, addr + cols) (relative to the block's
+// allocation; the lane bits of addr are ignored) must lie in [lo, hi) and
+// below the plan's column count.
+__device__ __forceinline__ void chk_tmem(const FusedParams& p, const Ctx& c, uint32_t addr,
+                                         uint32_t cols, uint32_t lo, uint32_t hi) {
+#ifdef NM_RANGE_CHECKS
+  const uint32_t col = (addr & 0xFFFFu) - (c.tmem & 0xFFFFu);
+  if (col < lo || col + cols > hi || col + cols > p.chk_tmem_cols)
+    atomicOr(p.status, kStatusRangeCheck);
+#else
+  (void)p, (void)c, (void)addr, (void)cols, (void)lo, (void)hi;
+#endif
+}
+
+// Tile slot s's accumulator columns, its A columns, and the ones column.
+__device__ __forceinline__ void chk_acc(const FusedParams& p, const Ctx& c, uint32_t s,
+                                        uint32_t addr, uint32_t cols) {
+  chk_tmem(p, c, addr, cols, s * p.slot_cols, s * p.slot_cols + p.a_col);
+}
+__device__ __forceinline__ void chk_a(const FusedParams& p, const Ctx& c, uint32_t s,
+                                      uint32_t addr, uint32_t cols) {
+  chk_tmem(p, c, addr, cols, s * p.slot_cols + p.a_col, (s + 1u) * p.slot_cols);
+}
+__device__ __forceinline__ void chk_ones(const FusedParams& p, const Ctx& c) {
+  chk_tmem(p, c, c.tmem + p.ones_col, 8u, p.ones_col, p.ones_col + 32u);
+}
+
+__device__ __forceinline__ void chk_smem(const FusedParams& p, const Ctx& c, uint32_t addr,
+                                         uint32_t bytes) {
+#ifdef NM_RANGE_CHECKS
+  if (addr < c.sbase || addr + bytes > c.sbase + p.smem_end) atomicOr(p.status, kStatusRangeCheck);
+#else
+  (void)p, (void)c, (void)addr, (void)bytes;
+#endif
+}
+
+// A copy of `bytes` into a buffer of `room` bytes.
+__device__ __forceinline__ void chk_fits(const FusedParams& p, uint32_t bytes, uint32_t room) {
+#ifdef NM_RANGE_CHECKS
+  if (bytes > room) atomicOr(p.status, kStatusRangeCheck);
+#else
+  (void)p, (void)bytes, (void)room;
+#endif
+}
+
+// Accumulator columns of an instruction descriptor (its N field).
+__device__ __forceinline__ uint32_t idesc_n(uint32_t idesc) { return ((idesc >> 17) & 0x3Fu) << 3; }
+
 // Bounded wait on an mbarrier phase. Gives up (and raises the abort flag and
 // the status word) when `limit_ns` passes or another role has given up. The
 // abort flag and the clock are looked at once every 64 polls (the clock
@@ -378,6 +432,7 @@ __device__ __forceinline__ void issue_input_tma(const FusedParams& p, uint32_t d
     uint32_t off;
     int w, k0;
     locate(kTileM, K, k, off, w, k0);
+    chk_fits(p, off + kTileM * 2u * static_cast<uint32_t>(w), p.in_stage_bytes);
     tma_load_2d(dst + off, &p.tm_in[swizzle_kind(w)], bar, k0, tile * kTileM);
     k = k0 + w;
   }
@@ -408,6 +463,7 @@ __device__ __forceinline__ void run_input_producer(const FusedParams& p, const C
                     p.status);
     if (!ok) break;
     mbar_arrive_expect_tx(c.bar(kBarInFull + st), tx);
+    chk_smem(p, c, c.sbase + p.sm_in + st * p.in_stage_bytes, p.in_stage_bytes);
     issue_input_tma(p, c.sbase + p.sm_in + st * p.in_stage_bytes, c.bar(kBarInFull + st), tile_of(i));
   }
   // Drain: the loads of the last D rounds of every slot (the latest fill of
@@ -498,6 +554,7 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
       uint32_t off;
       int w, k0;
       locate(static_cast<uint32_t>(N), K, col, off, w, k0);
+      chk_smem(p, c, b_stage + off + swz(static_cast<uint32_t>(n * 2 * w + (col - k0) * 2), w), 16u);
       st_shared_v4(b_stage + off + swz(static_cast<uint32_t>(n * 2 * w + (col - k0) * 2), w), v.x,
                    v.y, v.z, v.w);
     }
@@ -524,6 +581,17 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
     const LayerRegs li = load_layer(p, c, l);
     const uint32_t st = static_cast<uint32_t>(s) * D + static_cast<uint32_t>(rr) % D;
     const uint32_t in_base = c.sbase + p.sm_in + st * p.in_stage_bytes;
+    chk_acc(p, c, static_cast<uint32_t>(s), slot_tmem, idesc_n(li.idesc));
+    chk_ones(p, c);
+    if (l == 0) {
+      chk_smem(p, c, in_base, p.in_stage_bytes);
+    } else {
+      const uint32_t k_tm = (has_split_a(V) && static_cast<uint32_t>(li.K) > p.a_tmem_k)
+                                ? p.a_tmem_k : static_cast<uint32_t>(li.K);
+      chk_a(p, c, static_cast<uint32_t>(s), slot_tmem + p.a_col, k_tm >> 1);
+      if (has_split_a(V) && static_cast<uint32_t>(li.K) > p.a_tmem_k)
+        chk_smem(p, c, a_smem, 256u * (static_cast<uint32_t>(li.K) - p.a_tmem_k));
+    }
     bool ok = true;
     if (l == 0)
       ok = wait_phase(c.bar(kBarInFull + st), (static_cast<uint32_t>(rr) / D) & 1u, p.wait_ns,
@@ -681,16 +749,19 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
         tc_fence_after_sync();
         for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
           uint32_t acc[32];
+          chk_acc(p, c, static_cast<uint32_t>(s), tbase + static_cast<uint32_t>(c0), 32u);
           tmem_ld_x32(tbase + static_cast<uint32_t>(c0), acc);
           tmem_wait_ld();
           if constexpr (is_fp8(V)) {
             uint32_t q[8];
             convert_pairs_e4m3<16>(acc, slope2, q);
+            chk_a(p, c, static_cast<uint32_t>(s), a_tmem + static_cast<uint32_t>(c0 >> 2), 8u);
             tmem_st_x8(a_tmem + static_cast<uint32_t>(c0 >> 2), q);
           } else {
             uint32_t h[16];
             convert_pairs<V, 16, true>(acc, slope2, h);
             if (!has_split_a(V) || static_cast<uint32_t>(c0) < p.a_tmem_k) {
+              chk_a(p, c, static_cast<uint32_t>(s), a_tmem + static_cast<uint32_t>(c0 >> 1), 16u);
               tmem_st_x16(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
             } else {
               // this row's 64 bytes of the chunk, into the 128-byte-swizzled
@@ -699,9 +770,11 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
               const uint32_t kk = static_cast<uint32_t>(c0) - p.a_tmem_k;
               const uint32_t base = a_smem + (kk >> 6) * (kTileM * 128u);
 #pragma unroll
-              for (int cc = 0; cc < 4; ++cc)
+              for (int cc = 0; cc < 4; ++cc) {
+                chk_smem(p, c, base + swz(row * 128u + (kk & 63u) * 2u + 16u * cc, 64), 16u);
                 st_shared_v4(base + swz(row * 128u + (kk & 63u) * 2u + 16u * cc, 64), h[4 * cc],
                              h[4 * cc + 1], h[4 * cc + 2], h[4 * cc + 3]);
+              }
               a_in_smem = true;
             }
           }
@@ -710,9 +783,11 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
         if (!is_fp8(V) && (N & 31) && ((N >> 5) % G) == g) {
           const int c0 = N - 16;
           uint32_t acc[16], h[8];
+          chk_acc(p, c, static_cast<uint32_t>(s), tbase + static_cast<uint32_t>(c0), 16u);
           tmem_ld_x16(tbase + static_cast<uint32_t>(c0), acc);
           tmem_wait_ld();
           convert_pairs<V, 8, true>(acc, slope2, h);
+          chk_a(p, c, static_cast<uint32_t>(s), a_tmem + static_cast<uint32_t>(c0 >> 1), 8u);
           tmem_st_x8(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
         }
         if (V == kVarRowMajor) rebuild_b(l + 1);
@@ -753,26 +828,32 @@ __device__ __forceinline__ void run_slot(const FusedParams& p, const Ctx& c, int
         tc_fence_after_sync();
         for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
           uint32_t acc[32], h[16];
+          chk_acc(p, c, static_cast<uint32_t>(s), tbase + static_cast<uint32_t>(c0), 32u);
           tmem_ld_x32(tbase + static_cast<uint32_t>(c0), acc);
           tmem_wait_ld();
           convert_pairs<V, 16, false>(acc, slope2, h);
           const uint32_t base = out_dst + out_chunk_off(c0);
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
+          for (int cc = 0; cc < 4; ++cc) {
+            chk_smem(p, c, base + swz(row * 64u + cc * 16u, 32), 16u);
             st_shared_v4_nc(base + swz(row * 64u + cc * 16u, 32), h[4 * cc], h[4 * cc + 1],
                             h[4 * cc + 2], h[4 * cc + 3]);
+          }
         }
         if ((N & 31) && ((N >> 5) % G) == g) {
           const int c0 = N - 16;
           uint32_t acc[16], h[8];
+          chk_acc(p, c, static_cast<uint32_t>(s), tbase + static_cast<uint32_t>(c0), 16u);
           tmem_ld_x16(tbase + static_cast<uint32_t>(c0), acc);
           tmem_wait_ld();
           convert_pairs<V, 8, false>(acc, slope2, h);
           const uint32_t base = out_dst + out_chunk_off(c0);
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc)
+          for (int cc = 0; cc < 2; ++cc) {
+            chk_smem(p, c, base + swz(row * 32u + cc * 16u, 16), 16u);
             st_shared_v4_nc(base + swz(row * 32u + cc * 16u, 16), h[4 * cc], h[4 * cc + 1],
                             h[4 * cc + 2], h[4 * cc + 3]);
+          }
         }
         if (V == kVarRowMajor && (r + 1) * S + s < c.n_local) rebuild_b(0);
         fence_proxy_async_smem();  // staging tile -> TMA store (async proxy)
@@ -918,6 +999,9 @@ __device__ __forceinline__ void run_issuer(const FusedParams& p, const Ctx& c, i
       add(bd.b2);
       add(bd.b3);
     }
+    chk_acc(p, c, static_cast<uint32_t>(s), d, idesc_n(ip.idesc));
+    chk_a(p, c, static_cast<uint32_t>(s), a, 8u * ip.nslab);
+    chk_ones(p, c);
     group_ts(ip.nslab < 4u ? ip.nslab : 4u, d, a, 0u, bd, 0u, ip.idesc);
     for (uint32_t k0 = 4; k0 < ip.nslab; k0 += 4) {
       const PreDesc b = load_b4(ip.tab, k0);
@@ -939,6 +1023,8 @@ __device__ __forceinline__ void run_issuer(const FusedParams& p, const Ctx& c, i
                         c.abort_flag, p.status);
     };
     const uint32_t d = tmem_of(s);
+    chk_acc(p, c, static_cast<uint32_t>(s), d, idesc_n(li.idesc));
+    chk_smem(p, c, c.sbase + p.sm_in + st * p.in_stage_bytes, p.in_stage_bytes);
     if (!mma_chain_ss(nslab, d, c.slab_addr(p, 0u), a_add, b_base >> 4, li.idesc, wait))
       return false;
     umma_f16_ts(d, c.tmem + p.ones_col, smem_desc(c.sbase + p.sm_bslab + li.bslab_off, 256u, 6u),
@@ -1038,6 +1124,7 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
       uint32_t off;
       int w, k0;
       locate(static_cast<uint32_t>(N), K, col, off, w, k0);
+      chk_smem(p, c, b_stage + off + swz(static_cast<uint32_t>(n * 2 * w + (col - k0) * 2), w), 16u);
       st_shared_v4(b_stage + off + swz(static_cast<uint32_t>(n * 2 * w + (col - k0) * 2), w), v.x,
                    v.y, v.z, v.w);
     }
@@ -1061,17 +1148,21 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
         tc_fence_after_sync();
         for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
           uint32_t acc[32], h[16];
+          chk_acc(p, c, static_cast<uint32_t>(s), tbase + static_cast<uint32_t>(c0), 32u);
           tmem_ld_x32(tbase + static_cast<uint32_t>(c0), acc);
           tmem_wait_ld();
           convert_pairs<V, 16, true>(acc, slope2, h);
+          chk_a(p, c, static_cast<uint32_t>(s), a_tmem + static_cast<uint32_t>(c0 >> 1), 16u);
           tmem_st_x16(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
         }
         if ((N & 31) && ((N >> 5) % G) == g) {
           const int c0 = N - 16;
           uint32_t acc[16], h[8];
+          chk_acc(p, c, static_cast<uint32_t>(s), tbase + static_cast<uint32_t>(c0), 16u);
           tmem_ld_x16(tbase + static_cast<uint32_t>(c0), acc);
           tmem_wait_ld();
           convert_pairs<V, 8, true>(acc, slope2, h);
+          chk_a(p, c, static_cast<uint32_t>(s), a_tmem + static_cast<uint32_t>(c0 >> 1), 8u);
           tmem_st_x8(a_tmem + static_cast<uint32_t>(c0 >> 1), h);
         }
         if (V == kVarRowMajor) rebuild_b(l + 1);
@@ -1103,26 +1194,32 @@ __device__ __forceinline__ void run_epilogue(const FusedParams& p, const Ctx& c,
         tc_fence_after_sync();
         for (int c0 = 32 * g; c0 + 32 <= N; c0 += 32 * G) {
           uint32_t acc[32], h[16];
+          chk_acc(p, c, static_cast<uint32_t>(s), tbase + static_cast<uint32_t>(c0), 32u);
           tmem_ld_x32(tbase + static_cast<uint32_t>(c0), acc);
           tmem_wait_ld();
           convert_pairs<V, 16, false>(acc, slope2, h);
           const uint32_t base = out_dst + out_chunk_off(c0);
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
+          for (int cc = 0; cc < 4; ++cc) {
+            chk_smem(p, c, base + swz(row * 64u + cc * 16u, 32), 16u);
             st_shared_v4_nc(base + swz(row * 64u + cc * 16u, 32), h[4 * cc], h[4 * cc + 1],
                             h[4 * cc + 2], h[4 * cc + 3]);
+          }
         }
         if ((N & 31) && ((N >> 5) % G) == g) {
           const int c0 = N - 16;
           uint32_t acc[16], h[8];
+          chk_acc(p, c, static_cast<uint32_t>(s), tbase + static_cast<uint32_t>(c0), 16u);
           tmem_ld_x16(tbase + static_cast<uint32_t>(c0), acc);
           tmem_wait_ld();
           convert_pairs<V, 8, false>(acc, slope2, h);
           const uint32_t base = out_dst + out_chunk_off(c0);
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc)
+          for (int cc = 0; cc < 2; ++cc) {
+            chk_smem(p, c, base + swz(row * 32u + cc * 16u, 16), 16u);
             st_shared_v4_nc(base + swz(row * 32u + cc * 16u, 16), h[4 * cc], h[4 * cc + 1],
                             h[4 * cc + 2], h[4 * cc + 3]);
+          }
         }
         if (V == kVarRowMajor && (r + 1) * S + s < c.n_local) rebuild_b(0);
         fence_proxy_async_smem();  // staging tile -> TMA store (async proxy)
@@ -1173,6 +1270,8 @@ __device__ __forceinline__ void run_weight_producer(const FusedParams& p, const 
                         p.status);
         if (!ok) break;
         const uint32_t bytes = static_cast<uint32_t>(li.N) * 2u * static_cast<uint32_t>(w);
+        chk_smem(p, c, c.sbase + p.sm_wring + st * p.wstage_bytes, p.wstage_bytes);
+        chk_fits(p, bytes, p.wstage_bytes);
         mbar_arrive_expect_tx(c.bar(kBarWFull + st), bytes);
         bulk_load(c.sbase + p.sm_wring + st * p.wstage_bytes, p.blob + li.w_off + off, bytes,
                   c.bar(kBarWFull + st));
@@ -1250,6 +1349,7 @@ __global__ void __launch_bounds__(is_stream(V) ? 32 * (16 + 2) : 32 * kMaxReside
         row = j - p.bias_row0[l];
         v = gb[j];
       }
+      chk_smem(p, c, base + swz(row * 32u + ch * 16u, 16), 16u);
       st_shared_v4(base + swz(row * 32u + ch * 16u, 16), ch ? 0u : v, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
@@ -1483,6 +1583,8 @@ uint32_t plan_fused_smem(FusedParams& p, const int32_t* dims, int variant, uint3
               uint32_t cols = 32;
               while (cols < used) cols <<= 1;
               p.tmem_cols = cols;
+              p.chk_tmem_cols = used;
+              p.smem_end = off;
               p.ones_col = slots * p.slot_cols;
               p.n_slots = slots;
               // Issue groups: one tile region each, or (paired-tiles variant,

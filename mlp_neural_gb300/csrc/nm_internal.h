@@ -28,6 +28,9 @@ constexpr int kStreamSlots = 3;    // tile slots at most with streamed weights
 constexpr int kOutBufs = 2;        // output staging buffers per slot (TMA-store double buffer)
 constexpr int kMaxSlabs = kMaxLayers * (kMaxDim / 16);
 constexpr uint32_t kStatusTimeout = 1u;
+// Set by the checking build (NM_RANGE_CHECKS) when an address the kernel is
+// about to use falls outside the plan's tensor or shared memory.
+constexpr uint32_t kStatusRangeCheck = 2u;
 
 // Public variants 0..4 (nm_variant); 8 and 9 are the fused and the
 // scalar-activation kernels with streamed instead of resident weights, chosen
@@ -155,6 +158,10 @@ struct FusedParams {  // 128-byte aligned through its CUtensorMap members
   uint32_t stream_w;    // 1: weights streamed through the ring instead of resident
   uint32_t n_wstages;   // streamed-weight ring depth
   uint32_t wstage_bytes;
+  // Limits the checking build compares addresses against: the plan's TMEM
+  // columns (a test hook may lower it) and the end of its shared-memory
+  // layout (bytes from the 1024-aligned base).
+  uint32_t chk_tmem_cols, smem_end;
   uint64_t wait_ns;     // limit of every pipeline wait
   uint32_t test_stall;  // non-zero: the MMA thread first waits on kBarNever
 };

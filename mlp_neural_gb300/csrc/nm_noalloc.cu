@@ -149,5 +149,6 @@ extern "C" nm_status nm_mlp_infer_noalloc(const int32_t* dims, int32_t n_dims,
   uint32_t word = 0;
   if (cudaMemcpy(&word, status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
     return NM_ERR_CUDA;
+  if (word & nm::kStatusRangeCheck) return NM_ERR_RANGE_CHECK;
   return word ? NM_ERR_TIMEOUT : NM_OK;
 }

@@ -19,6 +19,7 @@ NM_ERR_NOT_PACKED = 3
 NM_ERR_OOM = 4
 NM_ERR_CUDA = 5
 NM_ERR_TIMEOUT = 6
+NM_ERR_RANGE_CHECK = 7
 
 NM_VARIANT_FUSED = 0
 NM_VARIANT_ROWMAJOR_WEIGHTS = 1
@@ -26,7 +27,11 @@ NM_VARIANT_SCALAR_ACTIVATION = 2
 NM_VARIANT_PAIRED_TILES = 3
 NM_VARIANT_FP8_WEIGHTS = 4
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnmmlp.so")
+# NM_CHECKED=1 in the environment selects the checking build
+# (libnmmlp_check.so, kernels compiled with NM_RANGE_CHECKS).
+_PKG = os.path.dirname(os.path.abspath(__file__))
+CHECKED = os.environ.get("NM_CHECKED", "") == "1"
+LIB_PATH = os.path.join(_PKG, "libnmmlp_check.so" if CHECKED else "libnmmlp.so")
 
 # Every symbol include/nm_mlp.h declares, with (restype, argtypes).
 _P = ctypes.c_void_p
@@ -46,6 +51,8 @@ SIGNATURES = {
     "nm_mlp_device_status": (ctypes.c_int, [_P, _P]),
     "nm_mlp_set_wait_limit": (ctypes.c_int, [_P, ctypes.c_uint64]),
     "nm_mlp_set_test_stall": (ctypes.c_int, [_P, ctypes.c_int32]),
+    "nm_checking_build": (ctypes.c_int32, []),
+    "nm_mlp_set_test_check_limit": (ctypes.c_int, [_P, ctypes.c_uint32]),
     "nm_mlp_infer_noalloc": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, _P, ctypes.c_int64, _P, _P]),
     "nm_mlp_plan": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int, ctypes.c_uint32, _P]),
     "nm_mlp_destroy": (None, [_P]),
@@ -62,15 +69,16 @@ class NmError(RuntimeError):
 
 
 def lib():
-    """Open libnmmlp.so (built by __graft_entry__.build() or
-    ``python -m mlp_neural_gb300.build``)."""
+    """Open libnmmlp.so, or libnmmlp_check.so under NM_CHECKED=1 (both built
+    by __graft_entry__.build(); ``python -m mlp_neural_gb300.build [--checked]``)."""
     global _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
                 raise RuntimeError(
                     f"{LIB_PATH} is missing: build it with "
-                    "`python -m mlp_neural_gb300.build` (there is no fallback path)")
+                    "`python -m mlp_neural_gb300.build"
+                    + (" --checked" if CHECKED else "") + "` (there is no fallback path)")
             L = ctypes.CDLL(LIB_PATH)
             for name, (res, args) in SIGNATURES.items():
                 fn = getattr(L, name)
@@ -243,3 +251,12 @@ class MLP:
 
     def set_test_stall(self, enable: bool):
         _check(lib().nm_mlp_set_test_stall(self._h, 1 if enable else 0), "nm_mlp_set_test_stall")
+
+    def set_test_check_limit(self, tmem_columns: int):
+        _check(lib().nm_mlp_set_test_check_limit(self._h, int(tmem_columns)),
+               "nm_mlp_set_test_check_limit")
+
+
+def checking_build() -> bool:
+    """nm_checking_build: True for the library compiled with NM_RANGE_CHECKS."""
+    return bool(lib().nm_checking_build())

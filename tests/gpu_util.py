@@ -12,8 +12,10 @@ TOL_REL = 1e-2
 
 
 def nm():
+    """The binding, its library built first (the checking build when the
+    process runs with NM_CHECKED=1)."""
     from mlp_neural_gb300 import build, nm as _nm
-    build.build()
+    build.build(checked=_nm.CHECKED)
     return _nm
 
 

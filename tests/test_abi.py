@@ -39,8 +39,25 @@ def test_library_exports_every_declared_symbol(nmlib):
     assert sorted(nmlib.SIGNATURES) == _declared_functions()
 
 
+def test_checking_build_exports_every_declared_symbol(nmlib):
+    """libnmmlp_check.so (NM_RANGE_CHECKS) builds, loads without a GPU,
+    exports the same calls and says which build it is."""
+    from mlp_neural_gb300 import build
+    path = build.build(checked=True)
+    L = ctypes.CDLL(path)
+    missing = [n for n in _declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+    L.nm_checking_build.restype = ctypes.c_int32
+    assert L.nm_checking_build() == 1
+    assert nmlib.lib().nm_checking_build() == 0
+    L.nm_mlp_set_test_check_limit.argtypes = [ctypes.c_void_p, ctypes.c_uint32]
+    assert L.nm_mlp_set_test_check_limit(None, 16) == nmlib.NM_ERR_INVALID_ARG
+    L.nm_status_str.restype = ctypes.c_char_p
+    assert L.nm_status_str(nmlib.NM_ERR_RANGE_CHECK) == b"NM_ERR_RANGE_CHECK"
+
+
 def test_status_strings(nmlib):
-    for code in range(7):
+    for code in range(8):
         assert nmlib.status_str(code).startswith("NM_")
     assert nmlib.status_str(nmlib.NM_ERR_TIMEOUT) == "NM_ERR_TIMEOUT"
     assert nmlib.lib().nm_abi_version() >= 1
