@@ -1068,6 +1068,9 @@ __device__ __forceinline__ void run_issuer(const FusedParams& p, const Ctx& c, i
         if (l + 1 < L) ip = prep_ts(l + 1);
         tc_fence_before_sync();
         named_bar_sync_lanes(bar_id, bar_threads);
+        // the epilogue's tcgen05.st of the next A (waited and fenced before
+        // the barrier) -> this warp's next MMAs, which read it
+        tc_fence_after_sync();
       }
     }
   }
