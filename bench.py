@@ -359,7 +359,7 @@ def main(argv=None):
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    nm_build.build()
+    nm_build.build(checked=nm.CHECKED)
     stream = torch.cuda.current_stream(dev)
 
     # network + one-time weight conversion (timed on its own, like the page's
@@ -547,7 +547,8 @@ def main(argv=None):
         "warmup": Wu, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": variant_dtype(args.variant), "data": "synthetic",
         "config": dict(workload_config(w), variant=args.variant, l2=l2_note,
-                       parallelism=f"replicas x{world}, no collective on the data path"),
+                       parallelism=f"replicas x{world}, no collective on the data path",
+                       **({"library": "checking build (NM_RANGE_CHECKS)"} if nm.CHECKED else {})),
         "roofline": roofline,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(hin.numel() * 2),
                 "d2h_bytes_per_step": int(hout.numel() * 2),
