@@ -283,10 +283,12 @@ nm_status nm_mlp_set_test_check_limit(nm_mlp *h, uint32_t tmem_columns);
  * whose work overlaps on the GPU -- from several host threads, or on several
  * streams -- race and must not be made.
  * The call returns after `stream` has completed the work (it synchronises the
- * stream), so a kernel-side give-up is reported directly as NM_ERR_TIMEOUT.
+ * stream), so a kernel-side give-up is reported directly as NM_ERR_TIMEOUT
+ * (and, in the checking build, a failed range check as NM_ERR_RANGE_CHECK).
  * Because it synchronises, it refuses a stream that is being captured into a
  * CUDA graph: it then returns NM_ERR_UNSUPPORTED before enqueuing anything.
- * Errors: NM_ERR_INVALID_ARG, NM_ERR_UNSUPPORTED, NM_ERR_CUDA, NM_ERR_TIMEOUT. */
+ * Errors: NM_ERR_INVALID_ARG, NM_ERR_UNSUPPORTED, NM_ERR_CUDA, NM_ERR_TIMEOUT,
+ * NM_ERR_RANGE_CHECK (checking build only). */
 nm_status nm_mlp_infer_noalloc(const int32_t *dims, int32_t n_dims, const void *const *W,
                                const void *const *b, const void *in, int64_t n, void *out,
                                nm_stream stream);
