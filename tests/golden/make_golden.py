@@ -32,9 +32,27 @@ def compute():
     return out
 
 
+def compute_fp8():
+    """The E4M3 pass (layers 2..L in E4M3) of the two wide networks, and a
+    SHA-256 of their E4M3 weight images."""
+    import hashlib
+    out = {}
+    for name in ("wide", "hetero"):
+        w = synth.WORKLOADS[name]
+        W, b = synth.net_params(w.dims, w.seed)
+        rows = {}
+        for r in ROWS:
+            x = synth.inputs(w, r, 1)
+            y = oracle.forward_fp8(w.dims, W, b, x)[0]
+            rows[str(r)] = [f"{int(v):04x}" for v in y]
+        images = hashlib.sha256(oracle.pack_fp8(w.dims, W).tobytes()).hexdigest()
+        out[name] = {"dims": list(w.dims), "seed": w.seed, "rows": rows, "images_sha256": images}
+    return out
+
+
 if __name__ == "__main__":
     path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "oracle_regression.json")
     with open(path, "w") as f:
-        json.dump({"generator": "tests/golden/make_golden.py (oracle only)", "workloads": compute()},
-                  f, indent=1)
+        json.dump({"generator": "tests/golden/make_golden.py (oracle only)", "workloads": compute(),
+                   "fp8_workloads": compute_fp8()}, f, indent=1)
     print("wrote", path)

@@ -50,3 +50,18 @@ def test_oracle_regression(orc):
         for r, hexes in rec["rows"].items():
             y = orc.forward(w.dims, W, b, synth.inputs(w, int(r), 1))[0]
             assert [f"{int(v):04x}" for v in y] == hexes, (name, r)
+
+
+def test_oracle_fp8_regression(orc):
+    """The oracle's E4M3 pass and its E4M3 images, against the stored values."""
+    import hashlib
+    g = _load("oracle_regression.json")["fp8_workloads"]
+    assert set(g) == {"wide", "hetero"}
+    for name, rec in g.items():
+        w = synth.WORKLOADS[name]
+        assert list(w.dims) == rec["dims"] and w.seed == rec["seed"]
+        W, b = synth.net_params(w.dims, w.seed)
+        assert hashlib.sha256(orc.pack_fp8(w.dims, W).tobytes()).hexdigest() == rec["images_sha256"]
+        for r, hexes in rec["rows"].items():
+            y = orc.forward_fp8(w.dims, W, b, synth.inputs(w, int(r), 1))[0]
+            assert [f"{int(v):04x}" for v in y] == hexes, (name, r)
