@@ -20,7 +20,7 @@ def _declared_functions():
 @pytest.fixture(scope="module")
 def nmlib():
     from mlp_neural_gb300 import build, nm
-    build.build()
+    build.build(checked=nm.CHECKED)
     return nm
 
 
@@ -49,7 +49,9 @@ def test_checking_build_exports_every_declared_symbol(nmlib):
     assert not missing, missing
     L.nm_checking_build.restype = ctypes.c_int32
     assert L.nm_checking_build() == 1
-    assert nmlib.lib().nm_checking_build() == 0
+    normal = ctypes.CDLL(build.build())
+    normal.nm_checking_build.restype = ctypes.c_int32
+    assert normal.nm_checking_build() == 0
     L.nm_mlp_set_test_check_limit.argtypes = [ctypes.c_void_p, ctypes.c_uint32]
     assert L.nm_mlp_set_test_check_limit(None, 16) == nmlib.NM_ERR_INVALID_ARG
     L.nm_status_str.restype = ctypes.c_char_p
@@ -99,3 +101,58 @@ def test_host_path_argument_checks_on_the_host(nmlib):
     L = nmlib.lib()
     assert L.nm_mlp_infer_host(None, None, 4, None, None) == nmlib.NM_ERR_INVALID_ARG
     assert L.nm_mlp_set_host_chunk(None, 0) == nmlib.NM_ERR_INVALID_ARG
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+#include "nm_mlp.h"
+
+int main(void) {
+    const int32_t page[9] = {48, 64, 64, 64, 64, 64, 64, 64, 16};
+    const int32_t bad[2] = {32, 24};
+    nm_plan plan;
+    nm_mlp *h = (nm_mlp *)1;
+    nm_status st;
+    printf("abi %d\n", (int)nm_abi_version());
+    printf("str %s\n", nm_status_str(NM_ERR_RANGE_CHECK));
+    st = nm_mlp_create(bad, 2, &h);
+    printf("create_bad %d %d\n", (int)st, h == NULL);
+    memset(&plan, 0, sizeof(plan));
+    st = nm_mlp_plan(page, 9, NM_VARIANT_FUSED, 232448u, &plan);
+    printf("plan %d %d %d %d %u\n", (int)st, (int)plan.tile_slots, (int)plan.threads,
+           (int)plan.streamed_weights, (unsigned)plan.tmem_columns);
+    printf("checking %d\n", (int)nm_checking_build());
+    nm_mlp_destroy(NULL);
+    return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(nmlib, tmp_path):
+    """A C99 program (gcc, -Wall -Werror -pedantic) includes the header, links
+    against the library and makes the calls that need no device: the boundary
+    holds for C callers, not only for the Python binding."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(nmlib.LIB_PATH)
+    lib = os.path.basename(nmlib.LIB_PATH)[3:-3]
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                        "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                        "-L", libdir, f"-l{lib}", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    out = dict(line.split(" ", 1) for line in r.stdout.strip().splitlines())
+    assert out["abi"] == "4"
+    assert out["str"] == "NM_ERR_RANGE_CHECK"
+    assert out["create_bad"] == "2 1"
+    assert out["plan"] == "0 5 896 0 512"
+    assert out["checking"] == ("1" if nmlib.CHECKED else "0")
