@@ -450,10 +450,18 @@ void free_host_stage(nm_mlp* h) {
 // stays short), at least 16,384 rows, at most 2^20, a multiple of 128.
 nm_status ensure_host_pipeline(nm_mlp* h) {
   if (!h->hs_start) {
+    // Each object is created once: after a failure part-way, a later call
+    // creates only what is still missing (nm_mlp_destroy frees what exists).
     for (int i = 0; i < kHostStreams; ++i) {
-      if (cudaStreamCreateWithFlags(&h->hs[i], cudaStreamNonBlocking) != cudaSuccess ||
-          cudaEventCreateWithFlags(&h->hs_done[i], cudaEventDisableTiming) != cudaSuccess)
+      if (!h->hs[i] && cudaStreamCreateWithFlags(&h->hs[i], cudaStreamNonBlocking) != cudaSuccess) {
+        h->hs[i] = nullptr;
         return NM_ERR_CUDA;
+      }
+      if (!h->hs_done[i] &&
+          cudaEventCreateWithFlags(&h->hs_done[i], cudaEventDisableTiming) != cudaSuccess) {
+        h->hs_done[i] = nullptr;
+        return NM_ERR_CUDA;
+      }
     }
     if (cudaEventCreateWithFlags(&h->hs_start, cudaEventDisableTiming) != cudaSuccess) {
       h->hs_start = nullptr;
