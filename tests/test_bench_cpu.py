@@ -46,3 +46,30 @@ def test_algorithmic_units_per_evaluation():
                              ("hetero", 337920, 160)]:
         w = synth.WORKLOADS[name]
         assert w.flops_per_eval == flops and w.hbm_bytes_per_eval == hbm
+
+
+def test_traffic_files_are_consistent():
+    """Every committed DRAM-traffic summary names its workload and variant as
+    its file does, its algorithmic bytes are the workload's (inputs and
+    outputs of a full launch), its total is read + write, its command runs
+    committed files only, and bench.py uses it exactly when it was taken on
+    the current kernel sources."""
+    import glob
+    import os
+    import re
+    files = sorted(glob.glob(os.path.join(bench.ROOT, "profiles", "fused_mlp_*.traffic.json")))
+    assert len(files) >= 5
+    for path in files:
+        d = json.load(open(path))
+        m = re.fullmatch(r"fused_mlp_([a-z0-9]+)_([a-z_]+)\.traffic\.json", os.path.basename(path))
+        assert m and (d["variant"], d["workload"]) == (m.group(1), m.group(2)), path
+        w = synth.WORKLOADS[d["workload"]]
+        assert d["algorithmic_bytes_per_launch"] == w.n_evals * w.hbm_bytes_per_eval, path
+        assert d["dram_bytes_per_launch"] == pytest.approx(
+            d["dram_bytes_read_per_launch"] + d["dram_bytes_write_per_launch"], abs=2), path
+        assert re.fullmatch(r"[0-9a-f]{64}", d["kernel_sources_sha256"])
+        assert "--clock-control none" in d["command"] and "python bench.py" in d["command"]
+        assert "_work" not in d["command"]
+        current = d["kernel_sources_sha256"] == bench.kernel_sources_sha()
+        got = bench.load_traffic(d["workload"], d["variant"])
+        assert got == (d["dram_bytes_per_launch"] if current else None), path
